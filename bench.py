@@ -1,0 +1,541 @@
+"""Benchmark of one tree-attention speculative verification step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload c2]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+tree_build_ancestry -> tree_attn_fwd -> tree_verify_greedy.  The metric is tree
+tokens verified per second (B * N / step time).  Prints ONE JSON line.
+
+Timing (impl=ours): the K timed steps are captured into CUDA graphs (chunks of
+S steps) with a timing event node around every library call, and replayed
+back to back; the whole timed region is bracketed by a barrier and a
+synchronize.  Steps rotate over several independent input sets whose union is
+larger than the 129 MB L2, so every step reads its inputs from HBM.  Per-kernel
+durations come from the event nodes of the last replayed chunk.  ``e2e``
+repeats the step through the same public calls from pinned host buffers, with
+the host->device copies of all inputs and the device->host read of the
+accepted path inside the timed region.  ``cpu_baseline`` (and impl=reference)
+time the CPU oracle on a bounded sample of the same workload.
+
+Under torchrun (--gpus N > 1) every rank runs an independent replica of the
+workload on its own GPU (the path has no exchange step); rank 0 prints the
+job-wide value = all ranks' tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def algorithmic(case) -> dict:
+    """Bytes each kernel must move and flops it must do for one step of ``case``."""
+    B, N, Hq, Hkv, D, W = case.B, case.N, case.Hq, case.Hkv, case.D, case.W
+    P = case.prefix_len.astype(np.int64)
+    anc_bytes = B * N * 4 + B * 4 + B * N * W * 8 + B * N * 8 + B * 4
+    nblk = int(sum(-(-int(p) // case.bs) for p in P))
+    attn_bytes = (int(P.sum()) * Hkv * D * 2 * 2 + B * N * Hq * D * 2 + B * N * Hkv * D * 2 * 2
+                  + B * N * W * 8 + nblk * 4 + B * 4 + B * N * Hq * D * 2 + B * N * Hq * 4)
+    # |A(i)| = depth + 1, counted here without the oracle: walk parent pointers
+    vis = 0
+    for b in range(B):
+        par = case.parent[b]
+        dep = np.zeros(N, np.int64)
+        for i in range(1, N):
+            dep[i] = dep[par[i]] + 1
+        vis += int(N * P[b] + (dep + 1).sum())
+    attn_flops = 4 * D * (Hq // Hkv) * Hkv * vis
+    ver_bytes = (B * N * case.vocab * 4 + 2 * B * N * 4 + B * N * 4 + B * 12) if case.vocab else 0
+    return {"tree_build_ancestry": {"bytes": anc_bytes, "flops": 0},
+            "tree_attn_fwd": {"bytes": attn_bytes, "flops": attn_flops},
+            "tree_verify_greedy": {"bytes": ver_bytes, "flops": 0}}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel's source changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.{workload}.traffic.txt")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip()
+    try:
+        srcs = rec["sources"].split()
+        h = hashlib.sha256()
+        for s in srcs:
+            h.update(open(os.path.join(ROOT, s), "rb").read())
+        if h.hexdigest()[:16] != rec["sources_sha256_16"]:
+            return None
+        return int(float(rec["dram_bytes_per_launch"]))
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.period = period_ms
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        def parse(s):
+            parts = [p.strip() for p in s.split(",")]
+            try:
+                return float(parts[0]), float(parts[1]), parts
+            except Exception:
+                return None
+
+        win = [(t, parse(s)) for t, s in self.samples if t0 <= t <= t1]
+        win = [(t, p) for t, p in win if p]
+        note = "samples inside the timed region"
+        if not win:   # a short timed region: take the samples closest to it
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[:3]
+            win = [(t, parse(s)) for t, s in near]
+            win = [(t, p) for t, p in win if p]
+            note = "no sample inside the timed region; nearest samples"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm = [p[0] for _, p in win]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in win:
+            for name, val in zip(names, p[2][4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(p[1] for _, p in win),
+                "reasons": sorted(reasons), "samples": len(win), "note": note}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a host float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample_step(case):
+    """One bounded oracle step: ancestry of every tree, attention of ONE
+    (sequence, kv-head) unit, argmax of a few logit rows and one acceptance
+    walk.  Returns (full-step seconds extrapolated by unit and row counts,
+    seconds actually spent, description of the sample)."""
+    import oracle
+    units_total = case.B * case.Hkv
+    rows_total = case.B * case.N
+    t0 = time.perf_counter()
+    oracle.tree.build_ancestry(case.parent, case.prefix_len)
+    t1 = time.perf_counter()
+    oracle.attention.tree_attention_case(case, units=[(0, 0)])
+    t2 = time.perf_counter()
+    t_ver = 0.0
+    vrows = 0
+    if case.vocab:
+        vrows = min(rows_total, 8)
+        lg = case.logits.reshape(rows_total, case.vocab)[:vrows]
+        oracle.verify.greedy_argmax(lg)
+        am = oracle.verify.greedy_argmax(case.logits[0])
+        oracle.verify.accept_walk(case.parent[0], case.draft[0], am, case.N)
+        t_ver = time.perf_counter() - t2
+    full = (t1 - t0) + (t2 - t1) * units_total + (t_ver * rows_total / max(vrows, 1) if vrows else 0.0)
+    desc = (f"ancestry of all {case.B} trees; attention of 1 of {units_total} (sequence, kv-head) units x "
+            f"{units_total}; argmax of {vrows} of {rows_total} logit rows (+ one acceptance walk) x "
+            f"{rows_total // max(vrows, 1)}")
+    return full, (t2 - t0) + t_ver, desc
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def time_oracle(case, budget_s: float, steps: int = 0):
+    """Repeat the bounded oracle step for about ``budget_s`` seconds (or exactly
+    ``steps`` times); tokens/s = B*N / extrapolated full-step time."""
+    est = []
+    spent = 0.0
+    desc = ""
+    n = 0
+    while (steps and n < steps) or (not steps and (spent < budget_s or n < 1)):
+        full, wall, desc = oracle_sample_step(case)
+        est.append(full)
+        spent += wall
+        n += 1
+    t = float(np.median(est))
+    return case.B * case.N / t, t, desc, n
+
+
+# ----------------------------------------------------------------------------- GPU bench
+
+def run_ours(args, world, rank, local):
+    import torch
+    import workloads as W
+    from tree_attention_speculative_gb300 import _build
+    _build.build()
+    from tree_attention_speculative_gb300.step import TreeVerifyStep
+    from tests.gpu_util import to_dev
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    base = W.make(args.workload)
+    set_bytes = sum(x.nbytes for x in (base.q, base.k_cache, base.v_cache, base.k_tree, base.v_tree)) + \
+        (base.logits.nbytes if base.logits is not None else 0)
+    nsets = max(1, min(16, math.ceil(2 * L2_BYTES / set_bytes))) if set_bytes < 2 * L2_BYTES else 1
+    cases = [base] + [W.make(args.workload, seed=20270000 + 97 * k) for k in range(1, nsets)]
+    dsets = [to_dev(c, dev) for c in cases]
+    # one set of output buffers per input set (prefix lengths, hence the split plan, may differ)
+    steps = [TreeVerifyStep(c.B, c.N, c.Hq, c.Hkv, c.D, c.prefix_len, vocab=c.vocab, max_depth=c.N - 1,
+                            device=dev) for c in cases]
+    step = steps[0]
+
+    def enqueue(k, evs=None):
+        t = dsets[k % nsets]
+        st = steps[k % nsets]
+        if evs: evs[0].record()
+        st.ancestry(t["parent"], t["prefix_len"])
+        if evs: evs[1].record()
+        st.attention(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["prefix_len"], t["k_tree"],
+                     t["v_tree"])
+        if evs: evs[2].record()
+        if base.vocab:
+            st.verify(t["draft"], t["logits"], t["parent"])
+        if evs: evs[3].record()
+
+    # allocate workspaces eagerly, then warm up
+    for k in range(nsets):
+        enqueue(k)
+    torch.cuda.synchronize()
+    for k in range(args.warmup):
+        enqueue(k)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    S = min(K, max(nsets, 8 * nsets))
+    S = S - S % nsets if S >= nsets else S
+    stream = torch.cuda.Stream(device=dev)
+
+    def capture(nsteps):
+        g = torch.cuda.CUDAGraph()
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(nsteps)]
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(nsteps):
+                enqueue(k, evs[k])
+        return g, evs
+
+    full, last = divmod(K, S)
+    g_main, ev_main = capture(S) if full else (None, None)
+    g_rem, ev_rem = capture(last) if last else (None, None)
+    # one untimed replay of each graph uploads it
+    if g_main: g_main.replay()
+    if g_rem: g_rem.replay()
+    torch.cuda.synchronize()
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for _ in range(full):
+        g_main.replay()
+    if g_rem:
+        g_rem.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier(world)
+    time.sleep(0.2)
+    sampler.stop()
+    ms_total = e0.elapsed_time(e1)
+    ms_total = max_over_ranks(ms_total, world, dev)
+    ms_step = ms_total / K
+
+    evs = ev_main if ev_main else ev_rem
+    per = {"tree_build_ancestry": [], "tree_attn_fwd": [], "tree_verify_greedy": []}
+    for e in evs:
+        per["tree_build_ancestry"].append(e[0].elapsed_time(e[1]))
+        per["tree_attn_fwd"].append(e[1].elapsed_time(e[2]))
+        if base.vocab:
+            per["tree_verify_greedy"].append(e[2].elapsed_time(e[3]))
+    kern_ms = {k: float(np.mean(v)) for k, v in per.items() if v}
+
+    # the timed steps must have run clean
+    for st in steps:
+        assert (st.status.cpu().numpy() == 0).all(), "timed step reported an error status"
+
+    # ---------------- e2e through the public calls, from pinned host buffers
+    import torch as _t
+    host = []
+    for c in cases:
+        h = {}
+        for name, arr in (("parent", c.parent), ("prefix_len", c.prefix_len), ("block_table", c.block_table)):
+            h[name] = _t.from_numpy(np.ascontiguousarray(arr, np.int32)).pin_memory()
+        for name in ("q", "k_cache", "v_cache", "k_tree", "v_tree"):
+            h[name] = _t.from_numpy(np.ascontiguousarray(getattr(c, name)).view(np.int16)).pin_memory()
+        if c.vocab:
+            h["draft"] = _t.from_numpy(np.ascontiguousarray(c.draft, np.int32)).pin_memory()
+            h["logits"] = _t.from_numpy(c.logits).pin_memory()
+        host.append(h)
+    outs = {"accepted": _t.empty((base.B, base.N), dtype=_t.int32).pin_memory(),
+            "accept_len": _t.empty(base.B, dtype=_t.int32).pin_memory(),
+            "bonus": _t.empty(base.B, dtype=_t.int32).pin_memory(),
+            "status": _t.empty(base.B, dtype=_t.int32).pin_memory()}
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    K_e2e = min(K, max(3 * nsets, int(2.0e-3 * K) + 3 * nsets)) if K > 200 else K
+
+    def e2e_step(k):
+        h = host[k % nsets]
+        t = dsets[k % nsets]
+        for name, src in h.items():
+            dst = t[name]
+            dst.view(_t.int16 if dst.dtype == _t.bfloat16 else dst.dtype).copy_(src, non_blocking=True)
+        enqueue(k)
+        st = steps[k % nsets]
+        if base.vocab:
+            outs["accepted"].copy_(st.accepted, non_blocking=True)
+            outs["accept_len"].copy_(st.accept_len, non_blocking=True)
+            outs["bonus"].copy_(st.bonus, non_blocking=True)
+        outs["status"].copy_(st.status, non_blocking=True)
+
+    for k in range(min(3, K_e2e)):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record()
+    for k in range(K_e2e):
+        e2e_step(k)
+    x1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_e2e = max_over_ranks(x0.elapsed_time(x1), world, dev) / K_e2e
+
+    tokens = base.B * base.N
+    value = world * tokens / (ms_step * 1e-3)
+    e2e_value = world * tokens / (ms_e2e * 1e-3)
+
+    alg = algorithmic(base)
+    pk = peaks()
+    dom = max(kern_ms, key=kern_ms.get)
+    a = alg[dom]
+    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    t_dom = kern_ms[dom] * 1e-3
+    if a["flops"] and a["flops"] / max(a["bytes"], 1) > ridge:
+        roof = {"bound": "tensor", "achieved": a["flops"] / t_dom / 1e12, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": a["bytes"] / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(dom, args.workload)
+    roof["kernel"] = dom
+    roof["algorithmic_bytes"] = a["bytes"]
+    roof["algorithmic_flops"] = a["flops"]
+    roof["peak_source"] = f"{pk['source']} ({'burst' if roof['unit'] == 'GB/s' else 'sustained'})"
+
+    kernels = {}
+    for k, ms in kern_ms.items():
+        kb = alg[k]
+        kernels[k] = {"ms": ms, "share": ms / sum(kern_ms.values()), "GB/s": kb["bytes"] / (ms * 1e-3) / 1e9,
+                      "hbm_frac": kb["bytes"] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+        if kb["flops"]:
+            kernels[k]["TFLOP/s"] = kb["flops"] / (ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, t, desc, n = time_oracle(base, budget_s=args.cpu_budget)
+        cpu = {"value": v, "unit": "tree tokens/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{desc}; median of {n} repeats; numpy fp64 oracle, BLAS threads as reported"}
+
+    clocks = sampler.summary(w0, w1)
+    line = {
+        "metric": "tree-verify step: tree tokens verified/s",
+        "value": value, "unit": "tree tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: " + WORKLOAD_DESC[args.workload], "batch": base.B,
+                   "tree_nodes": base.N, "q_heads": base.Hq, "kv_heads": base.Hkv, "head_dim": base.D,
+                   "prefix": [int(x) for x in np.unique(base.prefix_len)][:4], "kv_block": base.bs,
+                   "vocab": base.vocab, "parallelism": f"replicas x{world}",
+                   "l2": f"{nsets} rotating input sets of {set_bytes / 2**20:.1f} MiB "
+                         f"({nsets * set_bytes / 2**20:.0f} MiB > 129 MiB L2)",
+                   "timing": f"CUDA graphs of {S} steps replayed back to back, CUDA events"},
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": {"value": e2e_value, "unit": "tree tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": K_e2e, "ms_per_step": ms_e2e},
+        "gpu_launches": K * (3 if base.vocab else 2) + K,   # ancestry + attention (2 kernels) + verify
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+WORKLOAD_DESC = {
+    "c1": "5-node demo tree, B1, prefix 16, 2 heads, D64, vocab 1000",
+    "c2": "Llama-3-8B-shaped layer, B1, 64-node depth-6 tree, 32q/8kv heads, D128, contiguous 4096 prefix, "
+          "verify over vocab 128256",
+    "c3": "batched serving, B16, prefixes U[1024,16384], 26-node [4,3,2,1,1] tree, 32q/8kv, D128, paged bs16",
+    "c4": "70B-shaped layer, B64, 64-node depth-8 trees, 64q/8kv, D128, paged bs16 prefix 8192, vocab 128256",
+    "c5": "long context, B4, prefix 131072, 192-node depth-10 tree, 32q/8kv, D128, paged bs64, vocab 128256",
+}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: rank 0 alone, on the host cores."""
+    if rank != 0:
+        return
+    import workloads as W
+    case = W.make(args.workload)
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_sample_step(case)
+    w0 = time.time()
+    v, t, desc, n = time_oracle(case, budget_s=0, steps=args.steps)
+    wall = time.time() - w0
+    line = {
+        "metric": "tree-verify step: tree tokens verified/s", "value": v, "unit": "tree tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": f"{args.workload}: " + WORKLOAD_DESC[args.workload]},
+        "cpu_baseline": {"kind": "oracle", "cores": blas_threads(), "value": v,
+                         "sample": f"{desc}; median of {n} steps; {wall:.1f} s wall"},
+        "e2e": {"value": v, "unit": "tree tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def default_steps(workload: str) -> int:
+    return {"c1": 20000, "c2": 20000, "c3": 2000, "c4": 200, "c5": 200}[workload]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="c2")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.steps <= 0:
+        args.steps = default_steps(args.workload) if args.impl == "ours" else 3
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+/*
+ * treespec.h — C ABI of the GB300 tree-attention speculative verification library.
+ *
+ * One verification step scores a flattened tree of N draft tokens per sequence
+ * in a single pass and then accepts the longest draft path the target model
+ * agrees with.  The library exposes that step as three calls, each a stream-
+ * ordered launch of hand-written sm_103a kernels:
+ *
+ *   tree_build_ancestry  ancestor bitmasks, depths and positions of the tree
+ *   tree_attn_fwd        attention of every tree node over the verified prefix
+ *                        (paged KV cache) plus its own ancestors and itself
+ *   tree_verify_greedy   greedy argmax of every node's logits and the
+ *                        parent-chain acceptance walk
+ *
+ * Sources (web pages on the method):
+ *   [P1] "Tree Attention", inferensys glossary.
+ *   [P2] "Tree Attention", zhongzhoutan-coder terms page.
+ *   [P3] "Speculative Tree Attention: How Multi-Candidate Draft Models and
+ *        Parallel Verification Deliver 4x LLM Speedups", premlal news.
+ *
+ * Conventions shared by every call
+ *   - Every pointer is a DEVICE pointer unless its name ends in _host.
+ *   - The caller owns every buffer, workspace included.  The library never
+ *     allocates, frees or keeps a pointer past the call.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and the call returns without synchronising.
+ *   - The return value reports what the host can check before launching:
+ *     null pointers, shapes, unsupported sizes, too small a workspace, and
+ *     launch errors.  Nothing is launched when it is not TS_OK.
+ *   - Data-dependent errors (an invalid tree, a block id outside the pool, an
+ *     internal wait that timed out) are written as a ts_status code into the
+ *     caller's per-sequence int32 `status` array on the device.  A call never
+ *     writes 0 there except tree_build_ancestry, which (re)initialises it, so
+ *     one status array can be threaded through a whole step and read once.
+ *   - Index tensors are int32, row-major, densely packed.  bf16 tensors are
+ *     16-bit brain-float, row-major, densely packed, 16-byte aligned.
+ *   - Supported sizes: 1 <= N <= 256 nodes (W = ceil(N/64) <= 4 mask words),
+ *     head_dim D in {64, 128}, Hq = G * Hkv with G in {1, 2, 4, 8, 16},
+ *     KV block size a multiple of 16 that divides 128 or is a multiple of 128.
+ *     Anything else returns TS_ERR_UNSUPPORTED.
+ */
+#ifndef TREESPEC_H_
+#define TREESPEC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TS_API __attribute__((visibility("default")))
+#else
+#define TS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int ts_status;
+
+enum {
+  TS_OK = 0,
+  TS_ERR_NULL = -1,         /* a required pointer is NULL */
+  TS_ERR_SHAPE = -2,        /* inconsistent sizes, misaligned pointer, output too short */
+  TS_ERR_BAD_TREE = -3,     /* parent array is not a topologically ordered single-root tree */
+  TS_ERR_UNSUPPORTED = -4,  /* sizes outside the supported set above */
+  TS_ERR_BAD_BLOCK = -5,    /* block table entry outside [0, num_blocks) for a used block */
+  TS_ERR_TIMEOUT = -6,      /* an internal pipeline wait gave up (kernel exited early) */
+  TS_ERR_CUDA = -7,         /* a CUDA runtime call failed */
+  TS_ERR_WORKSPACE = -8     /* workspace NULL or smaller than the *_workspace_size query */
+};
+
+/* A cudaStream_t, passed as an opaque pointer so that this header needs no CUDA headers. */
+typedef void* ts_stream;
+
+/* Human-readable name of a status code (static string, never NULL). */
+TS_API const char* ts_status_str(ts_status st);
+
+/*
+ * tree_build_ancestry — tree-causal mask, depths and positions.
+ *
+ * Defines the ancestry ("tree-causal") mask of [P1] Key Mechanisms > Modified
+ * Causal Attention Mask (a node sees its ancestral path to the root and
+ * itself, no sibling branch), [P2] How It Works (prefix, self and ancestors
+ * only), built as in [P3]'s code listing (build_tree_attention_mask: walk
+ * parent pointers to the root), and the "position bookkeeping" of [P2]
+ * Tradeoffs.
+ *
+ *   parent_idx  [B, N] int32.  Node 0 is the root (parent -1); every other node
+ *               i has 0 <= parent_idx[i] < i (topological flattening).
+ *   prefix_len  [B] int32, verified-prefix length P_b >= 0 of each sequence.
+ *   anc_mask    [B, N, W] uint64 out, W = ceil(N/64).  Bit (j mod 64) of word
+ *               (j div 64) of row i is set iff node j is i or an ancestor of i.
+ *               Bits for j >= N are zero.
+ *   depth       [B, N] int32 out, parent steps from the node to the root.
+ *   pos         [B, N] int32 out, P_b + depth (the root sits at position P_b).
+ *   status      [B] int32 out: TS_OK, or TS_ERR_BAD_TREE (then anc_mask, depth
+ *               and pos of that sequence are zero).
+ * Returns TS_ERR_NULL / TS_ERR_UNSUPPORTED (N outside [1, 256], B < 1) / TS_ERR_CUDA.
+ */
+TS_API ts_status tree_build_ancestry(const int32_t* parent_idx, const int32_t* prefix_len, int B, int N,
+                              uint64_t* anc_mask, int32_t* depth, int32_t* pos, int32_t* status,
+                              ts_stream stream);
+
+/*
+ * Arguments of tree_attn_fwd (all pointers device unless *_host).
+ *
+ *   q           [B, N, Hq, D] bf16, queries of the tree nodes.
+ *   k_cache,
+ *   v_cache     [num_blocks, Hkv, block_size, D] bf16, the paged verified-prefix
+ *               KV pool.  Prefix token t of sequence b, KV head g, is row
+ *               (t mod block_size) of block block_table[b, t div block_size].
+ *               A contiguous cache is the special case block_size = P,
+ *               block_table[b] = {b}.
+ *   block_table [B, max_blocks] int32; only the first ceil(P_b / block_size)
+ *               entries of row b are read.
+ *   prefix_len  [B] int32 device copy of P_b; prefix_len_host the same values
+ *               in host memory (used to plan the split of the prefix).
+ *   k_tree,
+ *   v_tree      [B, N, Hkv, D] bf16, keys/values of the tree nodes themselves.
+ *   anc_mask    [B, N, W] uint64 from tree_build_ancestry.
+ *   pos         [B, N] int32 from tree_build_ancestry (read only when rotary
+ *               embedding is requested; must be 0 = off in this version, the
+ *               inputs are taken as already positioned).
+ *   out         [B, N, Hq, D] bf16 out.
+ *   lse         [B, N, Hq] fp32 out (natural-log softmax normaliser) or NULL.
+ *   status      [B] int32, error codes are written here (or NULL: not reported).
+ *   scale       softmax scale; 0 selects 1/sqrt(D).
+ *   Query head h reads KV head h / G (G = Hq / Hkv, consecutive grouping).
+ */
+typedef struct ts_attn_params {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const int32_t* prefix_len_host;
+  const void* k_tree;
+  const void* v_tree;
+  const uint64_t* anc_mask;
+  const int32_t* pos;
+  void* out;
+  float* lse;
+  int32_t* status;
+  int B, N, Hq, Hkv, D;
+  int block_size, num_blocks, max_blocks;
+  float scale;
+  float rope_theta;
+} ts_attn_params;
+
+/*
+ * Bytes of device workspace tree_attn_fwd needs for these sizes (split-prefix
+ * partial results).  Host-only: launches nothing, safe without a GPU.
+ * Returns 0 for arguments tree_attn_fwd would reject.
+ */
+TS_API size_t tree_attn_workspace_size(const ts_attn_params* p);
+
+/*
+ * tree_attn_fwd — the attention layer of the batched verification pass
+ * ([P1] Key Mechanisms > Batched Parallel Verification: every node of the
+ * tree is scored in one pass, each attending to its own root path; [P2] How
+ * It Works: a node attends to the verified prefix, itself and its ancestors).
+ *
+ * For sequence b, node i, query head h (KV head g = h / G):
+ *   keys = prefix tokens 0..P_b-1  ++  tree nodes j with bit j of anc_mask[b,i]
+ *   out[b,i,h] = softmax(scale * q . k) . v over those keys, lse likewise.
+ *
+ * workspace: device buffer of at least tree_attn_workspace_size(p) bytes,
+ * 256-byte aligned, contents need not be initialised; it is scratch for this
+ * call only (calls sharing one workspace must be stream-ordered).
+ * Returns TS_ERR_NULL / TS_ERR_SHAPE / TS_ERR_UNSUPPORTED / TS_ERR_WORKSPACE /
+ * TS_ERR_CUDA; a block id outside the pool sets status[b] = TS_ERR_BAD_BLOCK
+ * (that block is read as zeros), a timed-out internal wait sets
+ * TS_ERR_TIMEOUT.
+ */
+TS_API ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
+                        ts_stream stream);
+
+/*
+ * Bytes of device workspace tree_verify_greedy needs (per-row partial argmax
+ * results and arrival counters).  Host-only.
+ */
+TS_API size_t tree_verify_workspace_size(int B, int N, int V);
+
+/*
+ * tree_verify_greedy — greedy target prediction and acceptance.
+ *
+ * [P3] code listing, verify_candidate_tree: the target's prediction at a node
+ * is the argmax of its logits.  [P1] Key Mechanisms > Multi-Token Acceptance &
+ * Rollback and [P2] How It Works: the longest valid path from the root is
+ * accepted, up to the first rejection.  A node's logits predict its children:
+ * node c >= 1 is accepted iff every node x on its chain up to the root
+ * satisfies draft_tokens[x] == argmax(target_logits[parent(x)]).  The root is
+ * the last verified token and is always accepted.  n* is the deepest accepted
+ * node (ties: smallest index).
+ *
+ *   draft_tokens  [B, N] int32 draft token id of each node (the root's is unused).
+ *   target_logits [B, N, V] fp32, finite; the argmax takes the first index on ties.
+ *   parent_idx    [B, N] int32 as for tree_build_ancestry.
+ *   accepted      [B, max_depth + 1] int32 out: node ids root .. n*, then -1.
+ *   accept_len    [B] int32 out: depth(n*), the number of accepted drafts.
+ *   bonus         [B] int32 out: argmax of n*'s logits, the target's next token.
+ *   argmax_out    [B, N] int32 out, every node's argmax (required).
+ *   status        [B] int32: TS_ERR_BAD_TREE for an invalid tree; TS_ERR_SHAPE
+ *                 when depth(n*) > max_depth (accepted row left all -1,
+ *                 accept_len and bonus still written).
+ *   workspace     at least tree_verify_workspace_size(B, N, V) bytes, 256-byte
+ *                 aligned, ZERO-FILLED before its first use; every call leaves
+ *                 it zero-filled again, so it can be reused by stream-ordered
+ *                 calls without clearing.
+ * Returns TS_ERR_NULL / TS_ERR_UNSUPPORTED (N outside [1, 256], V < 1,
+ * max_depth < 0) / TS_ERR_WORKSPACE / TS_ERR_CUDA.
+ */
+TS_API ts_status tree_verify_greedy(const int32_t* draft_tokens, const float* target_logits,
+                             const int32_t* parent_idx, int B, int N, int V, int max_depth,
+                             int32_t* accepted, int32_t* accept_len, int32_t* bonus,
+                             int32_t* argmax_out, int32_t* status, void* workspace,
+                             size_t workspace_bytes, ts_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREESPEC_H_ */

@@ -1,0 +1,49 @@
+"""Helpers for the GPU parity tests: move a ``workloads.Case`` to the device and
+run one verification step through the library's C ABI."""
+import numpy as np
+import torch
+
+ATOL = 1e-2   # |out - ref| <= ATOL + RTOL * |ref| for bf16 attention outputs
+RTOL = 1e-2
+LSE_ATOL = 1e-3
+
+
+def to_dev(case, dev="cuda"):
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(x):
+        return torch.from_numpy(np.ascontiguousarray(x, np.int32)).to(dev)
+
+    t = dict(parent=i32(case.parent), prefix_len=i32(case.prefix_len), q=bf(case.q), k_cache=bf(case.k_cache),
+             v_cache=bf(case.v_cache), block_table=i32(case.block_table), k_tree=bf(case.k_tree),
+             v_tree=bf(case.v_tree))
+    if case.logits is not None:
+        t["draft"] = i32(case.draft)
+        t["logits"] = torch.from_numpy(case.logits).to(dev)
+    return t
+
+
+def run_case(case, max_depth=None, scale=0.0):
+    from tree_attention_speculative_gb300.step import TreeVerifyStep
+    t = to_dev(case)
+    step = TreeVerifyStep(case.B, case.N, case.Hq, case.Hkv, case.D, case.prefix_len, vocab=case.vocab,
+                          max_depth=max_depth, scale=scale)
+    step.run(t["parent"], t["prefix_len"], t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["k_tree"],
+             t["v_tree"], t.get("draft"), t.get("logits"))
+    torch.cuda.synchronize()
+    return step, t
+
+
+def out_f64(step):
+    return step.out.float().cpu().numpy().astype(np.float64)
+
+
+def assert_close_attention(got, ref, what=""):
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first {idx.tolist()} "
+                             f"got {got[tuple(idx[0])]} ref {ref[tuple(idx[0])]} max err {err.max()}")

@@ -1,0 +1,138 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching a GPU.  None of
+these calls launches a kernel, so they run without a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ts():
+    from tree_attention_speculative_gb300 import _build
+    _build.build()
+    import tree_attention_speculative_gb300 as ts
+    ts.lib()
+    return ts
+
+
+def _header_symbols():
+    src = open(os.path.join(ROOT, "include", "treespec.h")).read()
+    return sorted(set(re.findall(r"TS_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)))
+
+
+def test_header_declares_the_expected_calls():
+    syms = _header_symbols()
+    for name in ("tree_build_ancestry", "tree_attn_fwd", "tree_verify_greedy"):
+        assert name in syms
+
+
+def test_library_exports_every_header_symbol(ts):
+    L = ts.lib()
+    syms = _header_symbols()
+    assert syms, "no declarations found"
+    for name in syms:
+        assert hasattr(L, name), name
+    assert sorted(ts.EXPORTS) == syms
+
+
+def test_status_strings(ts):
+    for code in range(-8, 1):
+        assert ts.ts_status_str(code)
+    assert "invalid tree" in ts.ts_status_str(-3)
+
+
+class _FakeTensor:
+    """Stands in for a device tensor on a GPU-less host: shape + a fake aligned address."""
+    def __init__(self, shape, addr=0x10000):
+        self.shape = shape
+        self._addr = addr
+
+    def data_ptr(self):
+        return self._addr
+
+    def cpu(self):
+        return self
+
+
+def _params(ts, B=2, N=26, Hq=32, Hkv=8, D=128, bs=16, P=(1000, 3000), **kw):
+    nblk = sum(-(-p // bs) for p in P)
+    maxb = max(-(-p // bs) for p in P)
+    f = _FakeTensor
+    args = dict(q=f((B, N, Hq, D)), k_cache=f((nblk, Hkv, bs, D)), v_cache=f((nblk, Hkv, bs, D)),
+                block_table=f((B, maxb)), prefix_len=f((B,)), prefix_len_host=np.array(P, np.int32),
+                k_tree=f((B, N, Hkv, D)), v_tree=f((B, N, Hkv, D)), anc_mask=f((B, N, 1)), pos=f((B, N)),
+                out=f((B, N, Hq, D)), lse=None, status=f((B,)))
+    args.update(kw)
+    return ts.attn_params(**args)
+
+
+def test_attn_workspace_query_and_plan(ts):
+    p = _params(ts)
+    n = ts.tree_attn_workspace_size(p)
+    assert n > 0 and n % 256 == 0
+    # partial outputs for at least one split of every output row
+    assert n >= 2 * 26 * 32 * 128 * 4
+
+
+@pytest.mark.parametrize("change,code", [
+    (dict(q=None), -1),
+    (dict(D=96), -4),
+    (dict(Hq=24, Hkv=8), -4),      # G = 3
+    (dict(Hq=30, Hkv=8), -2),      # not a multiple
+    (dict(N=257), -4),
+    (dict(bs=48), -4),
+    (dict(rope_theta=10000.0), -4),
+    (dict(misalign=True), -2),
+    (dict(neg_prefix=True), -2),
+])
+def test_attn_rejects_before_launch(ts, change, code):
+    change = dict(change)
+    if change.pop("misalign", False):
+        p = _params(ts)
+        p.q = 0x10002
+    elif change.pop("neg_prefix", False):
+        p = _params(ts, P=(5, -1))
+    elif "q" in change:
+        p = _params(ts)
+        p.q = None
+    else:
+        p = _params(ts)
+        for k, v in change.items():
+            setattr(p, k if k != "bs" else "block_size", v)
+    assert ts.tree_attn_workspace_size(p) == 0
+    ws = _FakeTensor((1,), 0x20000)
+    ws.numel = lambda: 1 << 30
+    ws.element_size = lambda: 1
+    st = ts.lib().tree_attn_fwd(ctypes.byref(p), ctypes.c_void_p(0x20000), 1 << 30, None)
+    assert st == code
+
+
+def test_attn_rejects_small_workspace(ts):
+    p = _params(ts)
+    need = ts.tree_attn_workspace_size(p)
+    assert ts.lib().tree_attn_fwd(ctypes.byref(p), ctypes.c_void_p(0x20000), need - 256, None) == -8
+    assert ts.lib().tree_attn_fwd(ctypes.byref(p), None, need, None) == -8
+    assert ts.lib().tree_attn_fwd(ctypes.byref(p), ctypes.c_void_p(0x20010), need, None) == -8
+
+
+def test_verify_and_ancestry_reject_before_launch(ts):
+    L = ts.lib()
+    a = ctypes.c_void_p(0x10000)
+    assert L.tree_build_ancestry(None, a, 1, 5, a, a, a, a, None) == -1
+    assert L.tree_build_ancestry(a, a, 1, 257, a, a, a, a, None) == -4
+    assert L.tree_build_ancestry(a, a, 0, 5, a, a, a, a, None) == -4
+    assert ts.tree_verify_workspace_size(1, 5, 1000) > 0
+    assert ts.tree_verify_workspace_size(1, 300, 1000) == 0
+    need = ts.tree_verify_workspace_size(4, 64, 128256)
+    args = [a, a, a, 4, 64, 128256, 8, a, a, a, a, a, a, need, None]
+    bad = list(args); bad[1] = None
+    assert L.tree_verify_greedy(*bad) == -1
+    bad = list(args); bad[6] = -1
+    assert L.tree_verify_greedy(*bad) == -4
+    bad = list(args); bad[13] = need - 1
+    assert L.tree_verify_greedy(*bad) == -8

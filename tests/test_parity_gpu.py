@@ -1,0 +1,269 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Integer outputs (ancestry words, depths, positions, argmax, accepted paths,
+lengths, bonus tokens, status codes) must match bit for bit.  Attention
+outputs are bf16 and must satisfy |out - ref| <= 1e-2 + 1e-2 |ref| against the
+fp64 oracle; the natural-log lse must be within 1e-3.
+Small cases are compared element by element; the five named workloads at full
+size are compared on every output row the oracle can afford (all rows for the
+small ones, seeded samples of (sequence, kv head) units for the large ones).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.gpu_util import LSE_ATOL, assert_close_attention, out_f64, run_case, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from tree_attention_speculative_gb300 import _build
+    _build.build()
+    import tree_attention_speculative_gb300 as ts
+    ts.lib()
+    torch.cuda.init()
+
+
+# --------------------------------------------------------------------------- ancestry
+
+def _anc_gpu(parent, prefix_len):
+    from tree_attention_speculative_gb300 import tree_build_ancestry
+    B, N = parent.shape
+    W_ = (N + 63) // 64
+    dev = "cuda"
+    anc = torch.full((B, N, W_), -7, dtype=torch.int64, device=dev)
+    depth = torch.full((B, N), -7, dtype=torch.int32, device=dev)
+    pos = torch.full((B, N), -7, dtype=torch.int32, device=dev)
+    status = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    tree_build_ancestry(torch.from_numpy(parent.astype(np.int32)).to(dev),
+                        torch.from_numpy(prefix_len.astype(np.int32)).to(dev), anc, depth, pos, status)
+    torch.cuda.synchronize()
+    return (anc.cpu().numpy().view(np.uint64), depth.cpu().numpy(), pos.cpu().numpy(), status.cpu().numpy())
+
+
+@pytest.mark.parametrize("n", [1, 2, 5, 31, 32, 33, 63, 64, 65, 127, 128, 129, 192, 200, 255, 256])
+def test_ancestry_random_trees_bit_exact(n):
+    g = W.rng(n, "anc")
+    parents = np.stack([W.tree_random_recursive(g, n), W.tree_chain(n), W.tree_star(n),
+                        W.tree_random_levels(g, n, 10)])
+    plen = np.array([0, 1, 131072, 4096], np.int32)
+    got = _anc_gpu(parents, plen)
+    ref = oracle.tree.build_ancestry(parents, plen)
+    for x, y in zip(got, ref):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_ancestry_worked_example_and_invalid_trees():
+    parents = np.array([[-1, 0, 0, 1, 2], [-1, 0, 0, 4, 2], [0, 0, 0, 1, 2], [-1, 0, -1, 1, 2],
+                        [-1, 0, 0, 1, 7]], np.int32)
+    plen = np.array([16, 16, 16, 16, 16], np.int32)
+    got = _anc_gpu(parents, plen)
+    ref = oracle.tree.build_ancestry(parents, plen)
+    for x, y in zip(got, ref):
+        np.testing.assert_array_equal(x, y)
+    assert got[0][0, :, 0].tolist() == [1, 3, 5, 11, 21]
+    assert got[3].tolist() == [0, -3, -3, -3, -3]
+
+
+# --------------------------------------------------------------------------- attention
+
+SMALL = [
+    # name, B, N, Hq, Hkv, D, prefixes, bs, tree
+    ("g4_ragged", 2, 37, 8, 2, 128, [0, 300], 16, "random"),
+    ("g1_d64", 1, 5, 2, 2, 64, [16], 16, "worked"),
+    ("g2_multi_tile", 3, 70, 4, 2, 128, [129, 1, 640], 32, "levels"),
+    ("g8_rows_over_tile", 2, 40, 16, 2, 128, [257, 96], 64, "random"),
+    ("g16", 1, 9, 16, 1, 64, [383], 128, "chain"),
+    ("w3_192_nodes", 1, 192, 2, 1, 128, [200], 16, "levels"),
+    ("w4_256_nodes", 1, 256, 1, 1, 64, [0], 16, "random"),
+    ("contiguous_2k", 2, 26, 8, 2, 128, [2048, 2048], 2048, "widths"),
+]
+
+
+def _small_case(name, B, N, Hq, Hkv, D, plens, bs, tree):
+    g = W.rng(len(name), name)
+    if tree == "random":
+        parent = np.stack([W.tree_random_recursive(g, N) for _ in range(B)])
+    elif tree == "levels":
+        parent = np.stack([W.tree_random_levels(g, N, 8) for _ in range(B)])
+    elif tree == "chain":
+        parent = W.tree_chain(N)
+    elif tree == "worked":
+        parent = W.tree_worked_example()
+    else:
+        parent = W.tree_from_widths([4, 3, 2, 1, 1])
+    permute = bs < max(max(plens), 1)
+    return W.build_case(name, 7, parent, plens, Hq=Hq, Hkv=Hkv, D=D, bs=bs, permute=permute)
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=[s[0] for s in SMALL])
+def test_attention_small_elementwise(spec):
+    case = _small_case(*spec)
+    step, _ = run_case(case)
+    ref, ref_lse = oracle.attention.tree_attention_case(case)
+    assert step.status.cpu().tolist() == [0] * case.B
+    assert_close_attention(out_f64(step), ref, spec[0])
+    np.testing.assert_allclose(step.lse.cpu().numpy(), ref_lse, rtol=0, atol=LSE_ATOL)
+
+
+def test_attention_hot_keys_softmax_range():
+    case = W.build_case("hot", 3, W.tree_random_levels(W.rng(1, "h"), 48, 6), [700, 1500], Hq=8, Hkv=2,
+                        D=128, bs=64, permute=True, hot_key_frac=0.05, hot_key_scale=8.0)
+    step, _ = run_case(case)
+    ref, ref_lse = oracle.attention.tree_attention_case(case)
+    assert_close_attention(out_f64(step), ref, "hot keys")
+    np.testing.assert_allclose(step.lse.cpu().numpy(), ref_lse, rtol=0, atol=LSE_ATOL)
+
+
+def test_attention_bad_block_id_reported():
+    case = _small_case("g4_ragged", 2, 37, 8, 2, 128, [0, 300], 16, "random")
+    case.block_table[1, 3] = case.num_blocks + 5
+    step, _ = run_case(case)
+    assert step.status.cpu().tolist() == [0, -5]
+
+
+def test_attention_deterministic():
+    case = _small_case("g2_multi_tile", 3, 70, 4, 2, 128, [129, 1, 640], 32, "levels")
+    s1, _ = run_case(case)
+    o1 = s1.out.clone()
+    s2, _ = run_case(case)
+    assert torch.equal(o1, s2.out)
+
+
+# --------------------------------------------------------------------------- verify
+
+def _verify_check(case, max_depth):
+    step, _ = run_case(case, max_depth=max_depth)
+    acc, L, bonus, am, st = oracle.verify.verify_greedy(case.draft, case.logits, case.parent, max_depth)
+    np.testing.assert_array_equal(step.argmax.cpu().numpy(), am)
+    np.testing.assert_array_equal(step.status.cpu().numpy(), st)
+    np.testing.assert_array_equal(step.accept_len.cpu().numpy(), L)
+    np.testing.assert_array_equal(step.bonus.cpu().numpy(), bonus)
+    np.testing.assert_array_equal(step.accepted.cpu().numpy(), acc)
+    _assert_tickets_zero(step, case.B, case.N)
+    return step, acc, L
+
+
+def _assert_tickets_zero(step, B, N):
+    """The arrival counters at the head of the verify workspace (B*N row counters,
+    then B sequence counters at the next 256-byte boundary) are back at zero."""
+    ws = step.ws_verify.cpu().numpy()
+    rows = 4 * B * N
+    seq0 = (rows + 255) // 256 * 256
+    assert not ws[:rows].any() and not ws[seq0:seq0 + 4 * B].any()
+
+
+@pytest.mark.parametrize("vocab", [13, 1000, 8192, 8193, 20000, 128256])
+def test_verify_planted(vocab):
+    g = W.rng(vocab, "v")
+    B, N = 5, 33
+    if vocab < 100:   # a chain: one child per node, so a small vocabulary can still plant
+        parents = np.stack([W.tree_chain(N)] * B)
+    else:
+        parents = np.stack([W.tree_random_levels(g, N, 6) for _ in range(B)])
+    plant = [0, 1, 3, 6, 2]
+    case = W.build_case("v", vocab, parents, [4] * B, Hq=1, Hkv=1, D=64, bs=16, permute=False,
+                        vocab=vocab, plant_len=plant)
+    step, acc, L = _verify_check(case, 6)
+    assert L.tolist() == plant
+
+
+def test_verify_ties_and_chunk_boundaries():
+    B, N, V = 2, 6, 3 * 8192 + 4
+    parent = W.tree_chain(N)
+    case = W.build_case("t", 1, parent, [4, 4], Hq=1, Hkv=1, D=64, bs=16, permute=False, vocab=V, plant_len=[2, 0])
+    lg = case.logits
+    lg[0, 3, :] = 0.0
+    lg[0, 3, 8191] = 5.0
+    lg[0, 3, 8192] = 5.0          # tie across a chunk boundary: first wins
+    lg[1, 0, V - 1] = 50.0
+    lg[1, 0, 2 * 8192] = 50.0     # tie between chunk 2's first and the row's last
+    lg[1, 2, :] = -1.0
+    lg[1, 2, 0] = -0.5
+    _verify_check(case, 5)
+
+
+def test_verify_path_too_long_and_bad_tree():
+    g = W.rng(3, "x")
+    parents = np.stack([W.tree_chain(12), W.tree_random_levels(g, 12, 5), W.tree_chain(12)])
+    case = W.build_case("t", 2, parents, [4] * 3, Hq=1, Hkv=1, D=64, bs=16, permute=False, vocab=300,
+                        plant_len=[11, 5, 2])
+    case.parent[2, 5] = 9          # invalid: parent after child
+    step, acc, L = _verify_check(case, 4)
+    assert step.status.cpu().tolist() == [-2, -2, -3]
+
+
+def test_verify_repeated_calls_reuse_workspace():
+    case = W.c1()
+    s1, _ = run_case(case, max_depth=4)
+    t = to_dev(case)
+    for _ in range(3):
+        s1.verify(t["draft"], t["logits"], t["parent"])
+    torch.cuda.synchronize()
+    assert s1.accepted.cpu().tolist() == [[0, 1, 3, -1, -1]]
+    _assert_tickets_zero(s1, case.B, case.N)
+
+
+# --------------------------------------------------------------------------- the named workloads
+
+def test_c1_full():
+    case = W.c1()
+    step, _ = run_case(case, max_depth=4)
+    ref, ref_lse = oracle.attention.tree_attention_case(case)
+    assert_close_attention(out_f64(step), ref, "c1")
+    np.testing.assert_allclose(step.lse.cpu().numpy(), ref_lse, rtol=0, atol=LSE_ATOL)
+    anc, dep, pos, st = oracle.tree.build_ancestry(case.parent, case.prefix_len)
+    np.testing.assert_array_equal(step.anc.cpu().numpy().view(np.uint64), anc)
+    np.testing.assert_array_equal(step.pos.cpu().numpy(), pos)
+    assert step.accepted.cpu().tolist() == [[0, 1, 3, -1, -1]]
+    assert step.accept_len.cpu().tolist() == [2]
+
+
+def test_c2_full():
+    case = W.c2()
+    step, _ = run_case(case, max_depth=6)
+    ref, ref_lse = oracle.attention.tree_attention_case(case)
+    assert_close_attention(out_f64(step), ref, "c2")
+    np.testing.assert_allclose(step.lse.cpu().numpy(), ref_lse, rtol=0, atol=LSE_ATOL)
+    acc, L, bonus, am, st = oracle.verify.verify_greedy(case.draft, case.logits, case.parent, 6)
+    np.testing.assert_array_equal(step.accepted.cpu().numpy(), acc)
+    np.testing.assert_array_equal(step.argmax.cpu().numpy(), am)
+    assert L.tolist() == case.planted_len.tolist()
+
+
+def _sampled_units(case, k, seed):
+    g = np.random.default_rng(seed)
+    units = {(int(b), int(h)) for b, h in zip(g.integers(0, case.B, k), g.integers(0, case.Hkv, k))}
+    units |= {(0, 0), (case.B - 1, case.Hkv - 1)}
+    return sorted(units)
+
+
+@pytest.mark.parametrize("name,k", [("c3", 6), ("c4", 4), ("c5", 3)])
+def test_named_workload_sampled(name, k):
+    case = W.make(name)
+    vocab = case.vocab
+    step, _ = run_case(case, max_depth=12 if vocab else None)
+    units = _sampled_units(case, k, 99)
+    ref, ref_lse = oracle.attention.tree_attention_case(case, units=units)
+    got = out_f64(step)
+    glse = step.lse.cpu().numpy()
+    G = case.G
+    for b, g in units:
+        hs = slice(g * G, (g + 1) * G)
+        assert_close_attention(got[b, :, hs], ref[b, :, hs], f"{name} unit {(b, g)}")
+        np.testing.assert_allclose(glse[b, :, hs], ref_lse[b, :, hs], rtol=0, atol=LSE_ATOL)
+    assert np.isfinite(got).all()
+    assert step.status.cpu().tolist() == [0] * case.B
+    anc, dep, pos, st = oracle.tree.build_ancestry(case.parent, case.prefix_len)
+    np.testing.assert_array_equal(step.anc.cpu().numpy().view(np.uint64), anc)
+    np.testing.assert_array_equal(step.pos.cpu().numpy(), pos)
+    if vocab:
+        acc, L, bonus, am, st = oracle.verify.verify_greedy(case.draft, case.logits, case.parent, 12)
+        np.testing.assert_array_equal(step.argmax.cpu().numpy(), am)
+        np.testing.assert_array_equal(step.accepted.cpu().numpy(), acc)
+        np.testing.assert_array_equal(step.bonus.cpu().numpy(), bonus)
+        assert L.tolist() == case.planted_len.tolist()

@@ -1,0 +1,152 @@
+"""Python binding of libtreespec (GB300 tree-attention speculative verification).
+
+Argument marshalling only: every function below forwards torch tensors'
+device pointers, sizes and the current CUDA stream to the C entry point of
+the same name in ``include/treespec.h`` and raises ``TreeSpecError`` on a
+non-zero status.  All work runs in the library's CUDA kernels; there is no
+other implementation behind these names, and the package refuses to work if
+the library has not been built (``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from ._build import LIB as LIB_PATH
+
+__all__ = [
+    "TreeSpecError", "lib", "ts_status_str", "tree_build_ancestry", "AttnParams", "attn_params",
+    "tree_attn_workspace_size", "tree_attn_fwd", "tree_verify_workspace_size", "tree_verify_greedy",
+    "STATUS",
+]
+
+STATUS = {
+    0: "TS_OK", -1: "TS_ERR_NULL", -2: "TS_ERR_SHAPE", -3: "TS_ERR_BAD_TREE", -4: "TS_ERR_UNSUPPORTED",
+    -5: "TS_ERR_BAD_BLOCK", -6: "TS_ERR_TIMEOUT", -7: "TS_ERR_CUDA", -8: "TS_ERR_WORKSPACE",
+}
+
+
+class TreeSpecError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({ts_status_str(status)})")
+
+
+class AttnParams(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("prefix_len", ctypes.c_void_p),
+        ("prefix_len_host", ctypes.c_void_p), ("k_tree", ctypes.c_void_p), ("v_tree", ctypes.c_void_p),
+        ("anc_mask", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("N", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("D", ctypes.c_int), ("block_size", ctypes.c_int), ("num_blocks", ctypes.c_int),
+        ("max_blocks", ctypes.c_int), ("scale", ctypes.c_float), ("rope_theta", ctypes.c_float),
+    ]
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+# every symbol include/treespec.h declares
+EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_fwd",
+           "tree_verify_workspace_size", "tree_verify_greedy")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libtreespec is not built ({LIB_PATH} missing); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.ts_status_str.argtypes = [i32]
+        L.ts_status_str.restype = ctypes.c_char_p
+        L.tree_build_ancestry.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp]
+        L.tree_build_ancestry.restype = i32
+        L.tree_attn_workspace_size.argtypes = [ctypes.POINTER(AttnParams)]
+        L.tree_attn_workspace_size.restype = sz
+        L.tree_attn_fwd.argtypes = [ctypes.POINTER(AttnParams), vp, sz, vp]
+        L.tree_attn_fwd.restype = i32
+        L.tree_verify_workspace_size.argtypes = [i32, i32, i32]
+        L.tree_verify_workspace_size.restype = sz
+        L.tree_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.tree_verify_greedy.restype = i32
+        _LIB = L
+    return _LIB
+
+
+def ts_status_str(status: int) -> str:
+    return lib().ts_status_str(int(status)).decode()
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise TreeSpecError(st, where)
+
+
+def tree_build_ancestry(parent_idx: torch.Tensor, prefix_len: torch.Tensor, anc_mask: torch.Tensor,
+                        depth: torch.Tensor, pos: torch.Tensor, status: torch.Tensor, stream=None) -> None:
+    """parent_idx [B,N] i32, prefix_len [B] i32 -> anc_mask [B,N,W] u64 (int64 tensor), depth, pos [B,N] i32, status [B] i32."""
+    B, N = parent_idx.shape
+    _check(lib().tree_build_ancestry(_p(parent_idx), _p(prefix_len), B, N, _p(anc_mask), _p(depth), _p(pos),
+                                     _p(status), _s(stream)), "tree_build_ancestry")
+
+
+def attn_params(q, k_cache, v_cache, block_table, prefix_len, prefix_len_host, k_tree, v_tree, anc_mask, pos,
+                out, lse=None, status=None, scale: float = 0.0, rope_theta: float = 0.0) -> AttnParams:
+    """Fill the C parameter block from tensors (shapes as in treespec.h).
+
+    ``prefix_len_host`` is a host int32 tensor/array; the returned object keeps
+    it alive.
+    """
+    B, N, Hq, D = q.shape
+    nblk, Hkv, bs, _ = k_cache.shape
+    host = np.ascontiguousarray(np.asarray(prefix_len_host.cpu() if torch.is_tensor(prefix_len_host)
+                                           else prefix_len_host, dtype=np.int32))
+    p = AttnParams(q=q.data_ptr(), k_cache=k_cache.data_ptr(), v_cache=v_cache.data_ptr(),
+                   block_table=block_table.data_ptr(), prefix_len=prefix_len.data_ptr(),
+                   prefix_len_host=host.ctypes.data, k_tree=k_tree.data_ptr(), v_tree=v_tree.data_ptr(),
+                   anc_mask=anc_mask.data_ptr(), pos=pos.data_ptr() if pos is not None else None,
+                   out=out.data_ptr(), lse=lse.data_ptr() if lse is not None else None,
+                   status=status.data_ptr() if status is not None else None,
+                   B=B, N=N, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, num_blocks=nblk,
+                   max_blocks=block_table.shape[1], scale=scale, rope_theta=rope_theta)
+    p._keep = (host,)
+    return p
+
+
+def tree_attn_workspace_size(params: AttnParams) -> int:
+    return int(lib().tree_attn_workspace_size(ctypes.byref(params)))
+
+
+def tree_attn_fwd(params: AttnParams, workspace: torch.Tensor, stream=None) -> None:
+    _check(lib().tree_attn_fwd(ctypes.byref(params), _p(workspace), workspace.numel() * workspace.element_size(),
+                               _s(stream)), "tree_attn_fwd")
+
+
+def tree_verify_workspace_size(B: int, N: int, V: int) -> int:
+    return int(lib().tree_verify_workspace_size(B, N, V))
+
+
+def tree_verify_greedy(draft_tokens, target_logits, parent_idx, max_depth: int, accepted, accept_len, bonus,
+                       argmax_out, status, workspace, stream=None) -> None:
+    B, N, V = target_logits.shape
+    _check(lib().tree_verify_greedy(_p(draft_tokens), _p(target_logits), _p(parent_idx), B, N, V, max_depth,
+                                    _p(accepted), _p(accept_len), _p(bonus), _p(argmax_out), _p(status),
+                                    _p(workspace), workspace.numel() * workspace.element_size(), _s(stream)),
+           "tree_verify_greedy")

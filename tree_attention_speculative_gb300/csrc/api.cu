@@ -1,0 +1,198 @@
+// C ABI: argument validation, split planning, launches.  See include/treespec.h.
+#include <cmath>
+#include <cstring>
+
+#include "internal.cuh"
+
+namespace ts {
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool supported_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
+
+// Host validation shared by the workspace query and the launch.  Touches no
+// device memory and makes no CUDA call.
+ts_status check_attn(const ts_attn_params* p) {
+  if (!p) return TS_ERR_NULL;
+  if (!p->q || !p->k_cache || !p->v_cache || !p->block_table || !p->prefix_len ||
+      !p->prefix_len_host || !p->k_tree || !p->v_tree || !p->anc_mask || !p->out)
+    return TS_ERR_NULL;
+  if (p->B < 1 || p->N < 1 || p->Hq < 1 || p->Hkv < 1 || p->num_blocks < 1 || p->max_blocks < 1 ||
+      p->block_size < 1)
+    return TS_ERR_SHAPE;
+  if (p->N > MAX_NODES) return TS_ERR_UNSUPPORTED;
+  if (p->D != 64 && p->D != 128) return TS_ERR_UNSUPPORTED;
+  if (p->Hq % p->Hkv != 0) return TS_ERR_SHAPE;
+  if (!supported_group(p->Hq / p->Hkv)) return TS_ERR_UNSUPPORTED;
+  const int bs = p->block_size;
+  if (bs % 16 != 0 || !((KV_TILE % bs == 0) || (bs % KV_TILE == 0))) return TS_ERR_UNSUPPORTED;
+  if (p->rope_theta != 0.f) return TS_ERR_UNSUPPORTED;
+  if (!(p->scale >= 0.f) || std::isinf(p->scale)) return TS_ERR_SHAPE;
+  for (int b = 0; b < p->B; ++b) {
+    const int P = p->prefix_len_host[b];
+    if (P < 0) return TS_ERR_SHAPE;
+    if (ceil_div(P, bs) > p->max_blocks) return TS_ERR_SHAPE;
+  }
+  if (!aligned16(p->q) || !aligned16(p->k_cache) || !aligned16(p->v_cache) || !aligned16(p->k_tree) ||
+      !aligned16(p->v_tree) || !aligned16(p->out))
+    return TS_ERR_SHAPE;
+  return TS_OK;
+}
+
+// Split plan: cut every unit's prefix into equal chunks of tiles so that the
+// grid holds about two CTAs per SM across all units and row tiles.
+AttnPlan plan_attn(const ts_attn_params* p) {
+  AttnPlan pl{};
+  const int G = p->Hq / p->Hkv;
+  pl.row_tiles = ceil_div(p->N * G, ROW_TILE);
+  long long total = 0;
+  int max_tiles = 0;
+  for (int b = 0; b < p->B; ++b) {
+    const int t = prefix_tiles(p->prefix_len_host[b]);
+    total += t;
+    max_tiles = t > max_tiles ? t : max_tiles;
+  }
+  total *= (long long)p->Hkv * pl.row_tiles;
+  const long long target = 2LL * PLAN_SMS;
+  long long chunk = (total + target - 1) / target;
+  if (chunk < 1) chunk = 1;
+  pl.chunk_tiles = (int)chunk;
+  pl.max_splits = 1;
+  for (int b = 0; b < p->B; ++b) {
+    const int ns = num_splits(p->prefix_len_host[b], pl.chunk_tiles);
+    pl.max_splits = ns > pl.max_splits ? ns : pl.max_splits;
+  }
+  const size_t rows = (size_t)p->B * p->N * p->Hq;
+  pl.part_o_bytes = round256((size_t)pl.max_splits * rows * p->D * sizeof(float));
+  pl.part_lse_bytes = round256((size_t)pl.max_splits * rows * sizeof(float));
+  pl.workspace_bytes = pl.part_o_bytes + pl.part_lse_bytes;
+  (void)max_tiles;
+  return pl;
+}
+
+struct VerifyPlan {
+  int chunks;
+  size_t part_v, part_i, row_ticket, seq_ticket, total;
+};
+
+VerifyPlan plan_verify(int B, int N, int V) {
+  VerifyPlan pl{};
+  pl.chunks = ceil_div(V, VERIFY_CHUNK);
+  const size_t parts = (size_t)B * N * pl.chunks;
+  // tickets first: they must start zeroed and stay zeroed between calls
+  pl.row_ticket = 0;
+  pl.seq_ticket = round256((size_t)B * N * sizeof(unsigned));
+  pl.part_v = pl.seq_ticket + round256((size_t)B * sizeof(unsigned));
+  pl.part_i = pl.part_v + round256(parts * sizeof(float));
+  pl.total = pl.part_i + round256(parts * sizeof(int32_t));
+  return pl;
+}
+
+}  // namespace
+}  // namespace ts
+
+using namespace ts;
+
+extern "C" {
+
+const char* ts_status_str(ts_status st) {
+  switch (st) {
+    case TS_OK: return "ok";
+    case TS_ERR_NULL: return "null pointer";
+    case TS_ERR_SHAPE: return "bad shape, alignment or output size";
+    case TS_ERR_BAD_TREE: return "invalid tree (need parent[0] == -1 and 0 <= parent[i] < i)";
+    case TS_ERR_UNSUPPORTED: return "unsupported size";
+    case TS_ERR_BAD_BLOCK: return "block table entry outside the KV pool";
+    case TS_ERR_TIMEOUT: return "internal wait timed out";
+    case TS_ERR_CUDA: return "CUDA error";
+    case TS_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+ts_status tree_build_ancestry(const int32_t* parent_idx, const int32_t* prefix_len, int B, int N,
+                              uint64_t* anc_mask, int32_t* depth, int32_t* pos, int32_t* status,
+                              ts_stream stream) {
+  if (!parent_idx || !prefix_len || !anc_mask || !depth || !pos || !status) return TS_ERR_NULL;
+  if (B < 1 || N < 1 || N > MAX_NODES) return TS_ERR_UNSUPPORTED;
+  cudaError_t e = launch_ancestry(parent_idx, prefix_len, B, N, anc_mask, depth, pos, status,
+                                  (cudaStream_t)stream);
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+size_t tree_attn_workspace_size(const ts_attn_params* p) {
+  if (check_attn(p) != TS_OK) return 0;
+  return plan_attn(p).workspace_bytes;
+}
+
+ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
+                        ts_stream stream) {
+  ts_status st = check_attn(p);
+  if (st != TS_OK) return st;
+  const AttnPlan pl = plan_attn(p);
+  if (!workspace || workspace_bytes < pl.workspace_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return TS_ERR_WORKSPACE;
+  AttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(p->q);
+  a.k_cache = static_cast<const __nv_bfloat16*>(p->k_cache);
+  a.v_cache = static_cast<const __nv_bfloat16*>(p->v_cache);
+  a.block_table = p->block_table;
+  a.prefix_len = p->prefix_len;
+  a.k_tree = static_cast<const __nv_bfloat16*>(p->k_tree);
+  a.v_tree = static_cast<const __nv_bfloat16*>(p->v_tree);
+  a.anc_mask = p->anc_mask;
+  a.out = static_cast<__nv_bfloat16*>(p->out);
+  a.lse = p->lse;
+  a.status = p->status;
+  char* ws = static_cast<char*>(workspace);
+  a.part_o = reinterpret_cast<float*>(ws);
+  a.part_lse = reinterpret_cast<float*>(ws + pl.part_o_bytes);
+  a.B = p->B; a.N = p->N; a.Hq = p->Hq; a.Hkv = p->Hkv; a.G = p->Hq / p->Hkv; a.D = p->D;
+  a.W = ceil_div(p->N, 64);
+  a.bs = p->block_size; a.num_blocks = p->num_blocks; a.max_blocks = p->max_blocks;
+  const float scale = p->scale == 0.f ? 1.f / std::sqrt((float)p->D) : p->scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.chunk_tiles = pl.chunk_tiles;
+  a.max_splits = pl.max_splits;
+  a.row_tiles = pl.row_tiles;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_attn(a, s) != cudaSuccess) return TS_ERR_CUDA;
+  if (launch_combine(a, s) != cudaSuccess) return TS_ERR_CUDA;
+  return TS_OK;
+}
+
+size_t tree_verify_workspace_size(int B, int N, int V) {
+  if (B < 1 || N < 1 || N > MAX_NODES || V < 1) return 0;
+  return plan_verify(B, N, V).total;
+}
+
+ts_status tree_verify_greedy(const int32_t* draft_tokens, const float* target_logits,
+                             const int32_t* parent_idx, int B, int N, int V, int max_depth,
+                             int32_t* accepted, int32_t* accept_len, int32_t* bonus,
+                             int32_t* argmax_out, int32_t* status, void* workspace,
+                             size_t workspace_bytes, ts_stream stream) {
+  if (!draft_tokens || !target_logits || !parent_idx || !accepted || !accept_len || !bonus ||
+      !argmax_out || !status)
+    return TS_ERR_NULL;
+  if (B < 1 || N < 1 || N > MAX_NODES || V < 1 || max_depth < 0) return TS_ERR_UNSUPPORTED;
+  const VerifyPlan pl = plan_verify(B, N, V);
+  if (!workspace || workspace_bytes < pl.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return TS_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  VerifyArgs a{};
+  a.draft = draft_tokens;
+  a.logits = target_logits;
+  a.parent = parent_idx;
+  a.B = B; a.N = N; a.V = V; a.max_depth = max_depth; a.chunks = pl.chunks;
+  a.accepted = accepted; a.accept_len = accept_len; a.bonus = bonus; a.argmax = argmax_out;
+  a.status = status;
+  a.row_ticket = reinterpret_cast<unsigned*>(ws + pl.row_ticket);
+  a.seq_ticket = reinterpret_cast<unsigned*>(ws + pl.seq_ticket);
+  a.part_v = reinterpret_cast<float*>(ws + pl.part_v);
+  a.part_i = reinterpret_cast<int32_t*>(ws + pl.part_i);
+  return launch_verify(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "treespec.h"
+
+namespace ts {
+
+// Prefix keys are processed in tiles of KV_TILE tokens; packed query rows in
+// tiles of ROW_TILE rows (one MMA M extent).
+constexpr int KV_TILE = 128;
+constexpr int ROW_TILE = 128;
+constexpr int MAX_NODES = 256;
+constexpr int PLAN_SMS = 152;  // GB300: the planner sizes grids for 152 SMs
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Number of prefix tiles of a sequence, and how many splits its prefix is cut
+// into when every split takes `chunk_tiles` tiles.  A sequence with no prefix
+// still has one split: it carries the tree block.  The tree block always rides
+// on the LAST split of a sequence.
+__host__ __device__ inline int prefix_tiles(int P) { return ceil_div(P, KV_TILE); }
+__host__ __device__ inline int num_splits(int P, int chunk_tiles) {
+  int t = prefix_tiles(P);
+  return t == 0 ? 1 : ceil_div(t, chunk_tiles);
+}
+
+// The prefix length a kernel may use for sequence b: the device value, clamped
+// to what the host planned for (grid, workspace) and to the block table's
+// width.  Returns true when no clamping was needed.  Kernels report a clamp as
+// TS_ERR_SHAPE so a disagreement between the device and host prefix lengths can
+// never drive an access outside the planned buffers.
+__host__ __device__ inline bool usable_prefix(int P, int chunk_tiles, int max_splits, int bs, int max_blocks,
+                                              int* out) {
+  long long cap = (long long)chunk_tiles * max_splits * KV_TILE;
+  const long long cap_blocks = (long long)max_blocks * bs;
+  if (cap_blocks < cap) cap = cap_blocks;
+  long long v = P < 0 ? 0 : P;
+  const bool ok = (P >= 0) && (v <= cap);
+  if (v > cap) v = cap;
+  *out = (int)v;
+  return ok;
+}
+
+// Everything a launch of the attention kernels needs (device pointers).
+struct AttnArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const __nv_bfloat16* k_tree;
+  const __nv_bfloat16* v_tree;
+  const uint64_t* anc_mask;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* status;
+  float* part_o;    // [max_splits, B*N*Hq, D] fp32, normalised partial outputs
+  float* part_lse;  // [max_splits, B*N*Hq] fp32, base-2 log-sum-exp of each partial
+  int B, N, Hq, Hkv, G, D, W;
+  int bs, num_blocks, max_blocks;
+  float scale_log2;  // softmax scale * log2(e)
+  int chunk_tiles;   // prefix tiles per split
+  int max_splits;
+  int row_tiles;     // ceil(N*G / ROW_TILE)
+};
+
+struct AttnPlan {
+  int chunk_tiles;
+  int max_splits;
+  int row_tiles;
+  size_t part_o_bytes;
+  size_t part_lse_bytes;
+  size_t workspace_bytes;
+};
+
+cudaError_t launch_ancestry(const int32_t* parent, const int32_t* prefix_len, int B, int N,
+                            uint64_t* anc, int32_t* depth, int32_t* pos, int32_t* status,
+                            cudaStream_t s);
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s);
+
+struct VerifyArgs {
+  const int32_t* draft;
+  const float* logits;
+  const int32_t* parent;
+  int B, N, V, max_depth, chunks;
+  int32_t* accepted;
+  int32_t* accept_len;
+  int32_t* bonus;
+  int32_t* argmax;
+  int32_t* status;
+  float* part_v;
+  int32_t* part_i;
+  unsigned* row_ticket;
+  unsigned* seq_ticket;
+};
+constexpr int VERIFY_THREADS = 256;
+constexpr int VERIFY_CHUNK = 8192;  // logits per CTA
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
+
+}  // namespace ts

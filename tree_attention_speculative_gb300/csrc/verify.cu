@@ -1,0 +1,213 @@
+// Greedy verification: vocab argmax of every node's logits fused with the
+// parent-chain acceptance walk.
+//
+// [P3] code listing, verify_candidate_tree (the target's greedy prediction is
+// the argmax of a node's logits); [P1] Key Mechanisms > Multi-Token Acceptance
+// & Rollback and [P2] How It Works (accept the longest valid root path, up to
+// the first rejection).  The listing's own flattened-index scan is not
+// tree-aware and is not followed: a node's logits predict its children, and a
+// node is accepted only if every edge on its chain to the root matches.
+//
+// Layout of the work: the logits of row (b, i) are cut into chunks of
+// VERIFY_CHUNK floats, one CTA per (row, chunk).  Each CTA streams its chunk
+// with 16-byte loads (all of a thread's loads are issued before any is used),
+// keeps a running (max, first index) per thread, and reduces it with warp
+// shuffles and one shared-memory step.  The last CTA to finish a row (an
+// atomicInc ticket that wraps back to 0) folds the row's chunk partials; the
+// last row to finish a sequence (a second wrapping ticket) runs the acceptance
+// walk for that sequence, one thread per node.  No CTA ever waits for another,
+// so nothing here can hang; the tickets return to zero by themselves.
+#include <cfloat>
+#include <climits>
+
+#include "internal.cuh"
+
+namespace ts {
+
+__device__ __forceinline__ void take_better(float& v, int& i, float v2, int i2) {
+  // larger value wins; equal values keep the smaller index (first occurrence)
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    take_better(v, i, v2, i2);
+  }
+}
+
+// Reduce (v, i) over the CTA; the result is valid in thread 0.
+__device__ __forceinline__ void block_argmax(float& v, int& i) {
+  __shared__ float sv[VERIFY_THREADS / 32];
+  __shared__ int si[VERIFY_THREADS / 32];
+  warp_argmax(v, i);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    sv[w] = v;
+    si[w] = i;
+  }
+  __syncthreads();
+  if (w == 0) {
+    v = (l < VERIFY_THREADS / 32) ? sv[l] : -INFINITY;
+    i = (l < VERIFY_THREADS / 32) ? si[l] : INT_MAX;
+    warp_argmax(v, i);
+  }
+}
+
+__global__ void __launch_bounds__(VERIFY_THREADS)
+k_verify(VerifyArgs a) {
+  const int row = blockIdx.x / a.chunks;
+  const int chunk = blockIdx.x - row * a.chunks;
+  const int b = row / a.N;
+  const float* x = a.logits + (size_t)row * a.V;
+  const int lo = chunk * VERIFY_CHUNK;
+  const int hi = min(a.V, lo + VERIFY_CHUNK);
+
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  const bool vec = ((reinterpret_cast<uintptr_t>(x + lo) & 15) == 0) && (((hi - lo) & 3) == 0);
+  if (vec) {
+    constexpr int PER = VERIFY_CHUNK / (4 * VERIFY_THREADS);  // float4 per thread in a full chunk
+    const float4* x4 = reinterpret_cast<const float4*>(x + lo);
+    const int n4 = (hi - lo) >> 2;
+    float4 r[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int e = threadIdx.x + k * VERIFY_THREADS;
+      r[k] = (e < n4) ? __ldcs(x4 + e) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int base = lo + 4 * (threadIdx.x + k * VERIFY_THREADS);
+      // indices grow with k and within the float4: strict '>' keeps the first maximum
+      if (r[k].x > bv) { bv = r[k].x; bi = base; }
+      if (r[k].y > bv) { bv = r[k].y; bi = base + 1; }
+      if (r[k].z > bv) { bv = r[k].z; bi = base + 2; }
+      if (r[k].w > bv) { bv = r[k].w; bi = base + 3; }
+    }
+  } else {
+    for (int e = lo + threadIdx.x; e < hi; e += VERIFY_THREADS) {
+      const float v = x[e];
+      if (v > bv) { bv = v; bi = e; }
+    }
+  }
+  // A thread that saw only -inf (or nothing) must not claim an index ahead of
+  // one that saw a real -inf at a smaller index: its INT_MAX sentinel loses ties.
+  block_argmax(bv, bi);
+
+  __shared__ int s_flag;
+  if (a.chunks > 1) {
+    if (threadIdx.x == 0) {
+      a.part_v[blockIdx.x] = bv;
+      a.part_i[blockIdx.x] = bi;
+      __threadfence();
+      const unsigned old = atomicInc(&a.row_ticket[row], (unsigned)(a.chunks - 1));
+      s_flag = (old == (unsigned)(a.chunks - 1));
+    }
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+    // last chunk of this row: fold the row's partials (chunks <= 32 per row is
+    // not assumed; a strided loop covers any count)
+    float v = -INFINITY;
+    int i = INT_MAX;
+    for (int c = threadIdx.x; c < a.chunks; c += VERIFY_THREADS) {
+      take_better(v, i, __ldcg(a.part_v + (size_t)row * a.chunks + c),
+                  __ldcg(a.part_i + (size_t)row * a.chunks + c));
+    }
+    __syncthreads();
+    block_argmax(v, i);
+    bv = v;
+    bi = i;
+  }
+  if (threadIdx.x == 0) {
+    a.argmax[row] = bi;
+    __threadfence();
+    const unsigned old = atomicInc(&a.seq_ticket[b], (unsigned)(a.N - 1));
+    s_flag = (old == (unsigned)(a.N - 1));
+  }
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+
+  // ---- acceptance walk for sequence b (this CTA saw every row of b finish) ----
+  __shared__ int s_par[MAX_NODES], s_draft[MAX_NODES], s_pred[MAX_NODES];
+  __shared__ int s_key[VERIFY_THREADS / 32];
+  const int N = a.N;
+  const int t = threadIdx.x;
+  bool ok = true;
+  if (t < N) {
+    const int p = a.parent[(size_t)b * N + t];
+    ok = (t == 0) ? (p == -1) : (p >= 0 && p < t);
+    s_par[t] = p;
+    s_draft[t] = a.draft[(size_t)b * N + t];
+    s_pred[t] = __ldcg(a.argmax + (size_t)b * N + t);
+  }
+  const int valid = __syncthreads_and(ok);
+  int32_t* acc_row = a.accepted + (size_t)b * (a.max_depth + 1);
+  if (!valid) {
+    for (int k = t; k <= a.max_depth; k += VERIFY_THREADS) acc_row[k] = -1;
+    if (t == 0) {
+      a.accept_len[b] = 0;
+      a.bonus[b] = 0;
+      a.status[b] = TS_ERR_BAD_TREE;
+    }
+    return;
+  }
+  // key = (depth << 16) | (0xFFFF - node) for accepted nodes: the maximum key
+  // is the deepest accepted node, smallest index on ties.  The root is always
+  // accepted, so the maximum is never the -1 of a rejected node.
+  int key = -1;
+  if (t < N) {
+    bool acc = true;
+    int d = 0, y = t;
+    while (y != 0) {
+      const int p = s_par[y];
+      acc = acc && (s_draft[y] == s_pred[p]);
+      y = p;
+      ++d;
+    }
+    if (acc) key = (d << 16) | (0xFFFF - t);
+  }
+  key = __reduce_max_sync(0xffffffffu, key);
+  if ((t & 31) == 0) s_key[t >> 5] = key;
+  __syncthreads();
+  if (t < 32) {
+    int k2 = (t < VERIFY_THREADS / 32) ? s_key[t] : -1;
+    k2 = __reduce_max_sync(0xffffffffu, k2);
+    if (t == 0) s_key[0] = k2;
+  }
+  __syncthreads();
+  const int best = s_key[0];
+  const int L = best >> 16;
+  const int nstar = 0xFFFF - (best & 0xFFFF);
+  const bool fits = L <= a.max_depth;
+  for (int k = t; k <= a.max_depth; k += VERIFY_THREADS)
+    if (!fits || k > L) acc_row[k] = -1;
+  if (t == 0) {
+    if (fits) {
+      int y = nstar;
+      for (int k = L; k >= 0; --k) {
+        acc_row[k] = y;
+        y = s_par[y];
+      }
+    } else {
+      a.status[b] = TS_ERR_SHAPE;
+    }
+    a.accept_len[b] = L;
+    a.bonus[b] = s_pred[nstar];
+  }
+}
+
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
+  const int grid = a.B * a.N * a.chunks;
+  k_verify<<<grid, VERIFY_THREADS, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ts

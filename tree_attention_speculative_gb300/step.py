@@ -1,0 +1,75 @@
+"""One verification step on the GPU: device buffers plus the three library calls.
+
+``TreeVerifyStep`` owns the output and workspace buffers (allocated with torch,
+which is only the allocator here) for fixed sizes and enqueues
+tree_build_ancestry -> tree_attn_fwd -> tree_verify_greedy on one stream.  Every
+computation happens in the library's kernels.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import (attn_params, tree_attn_fwd, tree_attn_workspace_size, tree_build_ancestry,
+               tree_verify_greedy, tree_verify_workspace_size)
+
+
+class TreeVerifyStep:
+    def __init__(self, B: int, N: int, Hq: int, Hkv: int, D: int, prefix_len_host, vocab: int = 0,
+                 max_depth: Optional[int] = None, device="cuda", scale: float = 0.0):
+        self.B, self.N, self.Hq, self.Hkv, self.D = B, N, Hq, Hkv, D
+        self.vocab = vocab
+        self.max_depth = N - 1 if max_depth is None else max_depth
+        self.scale = scale
+        self.device = torch.device(device)
+        self.prefix_len_host = np.ascontiguousarray(np.asarray(prefix_len_host, np.int32))
+        W = (N + 63) // 64
+        dev = self.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.anc = torch.zeros(B, N, W, dtype=torch.int64, device=dev)
+        self.depth = torch.zeros(B, N, **i32)
+        self.pos = torch.zeros(B, N, **i32)
+        self.status = torch.zeros(B, **i32)
+        self.out = torch.empty(B, N, Hq, D, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(B, N, Hq, dtype=torch.float32, device=dev)
+        self.ws_attn = None
+        if vocab > 0:
+            nb = tree_verify_workspace_size(B, N, vocab)
+            # zero-filled once; the verify kernel leaves its counters at zero
+            self.ws_verify = torch.zeros(nb, dtype=torch.uint8, device=dev)
+            self.accepted = torch.empty(B, self.max_depth + 1, **i32)
+            self.accept_len = torch.empty(B, **i32)
+            self.bonus = torch.empty(B, **i32)
+            self.argmax = torch.empty(B, N, **i32)
+
+    def _params(self, q, k_cache, v_cache, block_table, prefix_len, k_tree, v_tree):
+        return attn_params(q, k_cache, v_cache, block_table, prefix_len, self.prefix_len_host, k_tree, v_tree,
+                           self.anc, self.pos, self.out, self.lse, self.status, scale=self.scale)
+
+    def attn_workspace_bytes(self, q, k_cache, v_cache, block_table, prefix_len, k_tree, v_tree) -> int:
+        return tree_attn_workspace_size(self._params(q, k_cache, v_cache, block_table, prefix_len, k_tree, v_tree))
+
+    def ancestry(self, parent, prefix_len, stream=None):
+        tree_build_ancestry(parent, prefix_len, self.anc, self.depth, self.pos, self.status, stream)
+
+    def attention(self, q, k_cache, v_cache, block_table, prefix_len, k_tree, v_tree, stream=None):
+        p = self._params(q, k_cache, v_cache, block_table, prefix_len, k_tree, v_tree)
+        need = tree_attn_workspace_size(p)
+        if need == 0:
+            raise ValueError("tree_attn_fwd would reject these arguments")
+        if self.ws_attn is None or self.ws_attn.numel() < need:
+            self.ws_attn = torch.empty(need, dtype=torch.uint8, device=self.device)
+        tree_attn_fwd(p, self.ws_attn, stream)
+
+    def verify(self, draft, logits, parent, stream=None):
+        tree_verify_greedy(draft, logits, parent, self.max_depth, self.accepted, self.accept_len, self.bonus,
+                           self.argmax, self.status, self.ws_verify, stream)
+
+    def run(self, parent, prefix_len, q, k_cache, v_cache, block_table, k_tree, v_tree, draft=None, logits=None,
+            stream=None):
+        self.ancestry(parent, prefix_len, stream)
+        self.attention(q, k_cache, v_cache, block_table, prefix_len, k_tree, v_tree, stream)
+        if logits is not None:
+            self.verify(draft, logits, parent, stream)
