@@ -216,6 +216,43 @@ TS_API ts_status tree_verify_greedy(const int32_t* draft_tokens, const float* ta
                              int32_t* argmax_out, int32_t* status, void* workspace,
                              size_t workspace_bytes, ts_stream stream);
 
+/* Size of the library-owned scratch behind tree_verify_greedy_noalloc. */
+#define TS_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/*
+ * tree_verify_greedy_noalloc — tree_verify_greedy for callers that cannot
+ * allocate.  The pages have no counterpart to this call; it exists for users
+ * of this library that are not allowed to allocate device memory or are not
+ * given a workspace: a plugin inside another inference engine that receives
+ * only its input and output buffers, or a latency-critical loop in which a
+ * cudaMalloc (which may synchronise the whole device) is not acceptable.
+ *
+ * Arguments, outputs and status codes are those of tree_verify_greedy, minus
+ * the workspace.  The scratch is a fixed array of
+ * TS_VERIFY_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library; every GPU that
+ * loads the library holds it until the process exits.  Sizes whose scratch
+ * (tree_verify_workspace_size(B, N, V)) exceeds that limit return
+ * TS_ERR_WORKSPACE before anything is launched.  The need is about
+ * 8 * B*N * ceil(V / 8192) + 4 * (B*N + B) bytes: 0.5 MiB for B*N = 4096
+ * nodes over a 128256-token vocabulary, so the limit is B*N of about 30000
+ * nodes at that vocabulary.
+ *
+ * - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ * - The first call on a device looks up the array's device address (with the
+ *   device that owns `stream` current) and caches it; make that first call
+ *   before any stream capture.
+ * - Each call clears the scratch's arrival counters on `stream` (an async
+ *   memset) before its kernel; the array keeps the rest of the previous
+ *   call's contents.
+ * - Every call on a device shares the one array: calls that can overlap on
+ *   the GPU (different streams without ordering between them) race and give
+ *   wrong results.  Order them on one stream.
+ */
+TS_API ts_status tree_verify_greedy_noalloc(const int32_t* draft_tokens, const float* target_logits,
+                                            const int32_t* parent_idx, int B, int N, int V, int max_depth,
+                                            int32_t* accepted, int32_t* accept_len, int32_t* bonus,
+                                            int32_t* argmax_out, int32_t* status, ts_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ from ._build import LIB as LIB_PATH
 __all__ = [
     "TreeSpecError", "lib", "ts_status_str", "tree_build_ancestry", "AttnParams", "attn_params",
     "tree_attn_workspace_size", "tree_attn_fwd", "tree_verify_workspace_size", "tree_verify_greedy",
-    "STATUS",
+    "tree_verify_greedy_noalloc", "NOALLOC_SCRATCH_BYTES", "STATUS",
 ]
 
 STATUS = {
@@ -53,7 +53,10 @@ _LIB: Optional[ctypes.CDLL] = None
 
 # every symbol include/treespec.h declares
 EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_fwd",
-           "tree_verify_workspace_size", "tree_verify_greedy")
+           "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc")
+
+# TS_VERIFY_NOALLOC_SCRATCH_BYTES of treespec.h
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 def lib() -> ctypes.CDLL:
@@ -76,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.tree_verify_workspace_size.restype = sz
         L.tree_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.tree_verify_greedy.restype = i32
+        L.tree_verify_greedy_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.tree_verify_greedy_noalloc.restype = i32
         _LIB = L
     return _LIB
 
@@ -150,3 +155,17 @@ def tree_verify_greedy(draft_tokens, target_logits, parent_idx, max_depth: int, 
                                     _p(accepted), _p(accept_len), _p(bonus), _p(argmax_out), _p(status),
                                     _p(workspace), workspace.numel() * workspace.element_size(), _s(stream)),
            "tree_verify_greedy")
+
+
+def tree_verify_greedy_noalloc(draft_tokens, target_logits, parent_idx, max_depth: int, accepted, accept_len, bonus,
+                               argmax_out, status, stream=None) -> None:
+    """tree_verify_greedy without a workspace, for callers that may not allocate
+    device memory (e.g. a plugin handed only its input/output buffers).  Runs on
+    a fixed 4 MiB scratch array inside the library; larger problems raise
+    TS_ERR_WORKSPACE.  Calls on one device share that array, so keep them
+    ordered on one stream; make the first call on a device outside any stream
+    capture (it looks up the array's device address)."""
+    B, N, V = target_logits.shape
+    _check(lib().tree_verify_greedy_noalloc(_p(draft_tokens), _p(target_logits), _p(parent_idx), B, N, V, max_depth,
+                                            _p(accepted), _p(accept_len), _p(bonus), _p(argmax_out), _p(status),
+                                            _s(stream)), "tree_verify_greedy_noalloc")

@@ -195,4 +195,37 @@ ts_status tree_verify_greedy(const int32_t* draft_tokens, const float* target_lo
   return launch_verify(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
+ts_status tree_verify_greedy_noalloc(const int32_t* draft_tokens, const float* target_logits,
+                                     const int32_t* parent_idx, int B, int N, int V, int max_depth,
+                                     int32_t* accepted, int32_t* accept_len, int32_t* bonus,
+                                     int32_t* argmax_out, int32_t* status, ts_stream stream) {
+  if (!draft_tokens || !target_logits || !parent_idx || !accepted || !accept_len || !bonus ||
+      !argmax_out || !status)
+    return TS_ERR_NULL;
+  if (B < 1 || N < 1 || N > MAX_NODES || V < 1 || max_depth < 0) return TS_ERR_UNSUPPORTED;
+  const VerifyPlan pl = plan_verify(B, N, V);
+  if (pl.total > TS_VERIFY_NOALLOC_SCRATCH_BYTES) return TS_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  const ts_status st = verify_static_scratch(&scratch, &scratch_bytes);
+  if (st != TS_OK) return st;
+  if (pl.total > scratch_bytes) return TS_ERR_WORKSPACE;
+  // The array keeps whatever the previous call left; the arrival counters
+  // must start at zero, so clear them on the caller's stream.
+  if (cudaMemsetAsync(scratch, 0, pl.part_v, (cudaStream_t)stream) != cudaSuccess) return TS_ERR_CUDA;
+  char* ws = static_cast<char*>(scratch);
+  VerifyArgs a{};
+  a.draft = draft_tokens;
+  a.logits = target_logits;
+  a.parent = parent_idx;
+  a.B = B; a.N = N; a.V = V; a.max_depth = max_depth; a.chunks = pl.chunks;
+  a.accepted = accepted; a.accept_len = accept_len; a.bonus = bonus; a.argmax = argmax_out;
+  a.status = status;
+  a.row_ticket = reinterpret_cast<unsigned*>(ws + pl.row_ticket);
+  a.seq_ticket = reinterpret_cast<unsigned*>(ws + pl.seq_ticket);
+  a.part_v = reinterpret_cast<float*>(ws + pl.part_v);
+  a.part_i = reinterpret_cast<int32_t*>(ws + pl.part_i);
+  return launch_verify(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
 }  // extern "C"

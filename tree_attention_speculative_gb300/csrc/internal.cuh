@@ -101,5 +101,6 @@ struct VerifyArgs {
 constexpr int VERIFY_THREADS = 256;
 constexpr int VERIFY_CHUNK = 8192;  // logits per CTA
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
+ts_status verify_static_scratch(void** ptr, size_t* bytes);
 
 }  // namespace ts

@@ -19,6 +19,7 @@
 // so nothing here can hang; the tickets return to zero by themselves.
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 #include "internal.cuh"
 
@@ -208,6 +209,42 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   const int grid = a.B * a.N * a.chunks;
   k_verify<<<grid, VERIFY_THREADS, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Library-owned scratch for tree_verify_greedy_noalloc.
+//
+// Some callers cannot hand the library a workspace: plugins inside another
+// engine that only receive their input and output buffers, or code on a
+// latency-critical path where a cudaMalloc (which may synchronise the device)
+// is not allowed.  For them the verify kernel can run on this fixed array,
+// which every GPU that loads the library holds until the process exits.
+// Host code must not use the array's name as a pointer (on the host it names
+// a stand-in, not device memory): its device address is looked up once per
+// device with cudaGetSymbolAddress, with that device current.
+static __device__ __align__(256) unsigned char g_verify_scratch[TS_VERIFY_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+void* g_verify_scratch_addr[kMaxDevices] = {};
+std::mutex g_verify_scratch_mu;
+}  // namespace
+
+// Device address and size of the scratch array on the current device; the
+// first call on a device performs the lookup.
+ts_status verify_static_scratch(void** ptr, size_t* bytes) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return TS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_verify_scratch_mu);
+  if (!g_verify_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || !p) return TS_ERR_CUDA;
+    g_verify_scratch_addr[dev] = p;
+  }
+  *ptr = g_verify_scratch_addr[dev];
+  *bytes = sizeof(g_verify_scratch);
+  return TS_OK;
 }
 
 }  // namespace ts
