@@ -1,6 +1,7 @@
 // C ABI: argument validation, split planning, launches.  See include/treespec.h.
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "internal.cuh"
 
@@ -70,6 +71,24 @@ AttnPlan plan_attn(const ts_attn_params* p) {
   pl.workspace_bytes = pl.part_o_bytes + pl.part_lse_bytes;
   (void)max_tiles;
   return pl;
+}
+
+// The attention kernel's shared-memory opt-in, once per device (a host-side
+// attribute, so the first call should come before any stream capture).
+cudaError_t prepare_device() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    e = attn_tc_prepare();
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
 }
 
 struct VerifyPlan {
@@ -158,8 +177,10 @@ ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspa
   a.max_splits = pl.max_splits;
   a.row_tiles = pl.row_tiles;
   cudaStream_t s = (cudaStream_t)stream;
-  if (launch_attn(a, s) != cudaSuccess) return TS_ERR_CUDA;
-  if (launch_combine(a, s) != cudaSuccess) return TS_ERR_CUDA;
+  if (prepare_device() != cudaSuccess) return TS_ERR_CUDA;
+  if (launch_attn_tc(a, s) != cudaSuccess) return TS_ERR_CUDA;
+  // with one split per unit the kernel writes `out` itself; otherwise merge the splits
+  if (a.max_splits > 1 && launch_combine(a, s) != cudaSuccess) return TS_ERR_CUDA;
   return TS_OK;
 }
 

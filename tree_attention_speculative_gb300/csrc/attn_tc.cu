@@ -1,0 +1,493 @@
+// Tree attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes — [P1] Key Mechanisms > Batched Parallel Verification and
+// Modified Causal Attention Mask; [P2] How It Works: every tree node's query
+// attends to the whole verified prefix of its sequence and to the tree nodes
+// on its own root path (its ancestors and itself), in one pass.
+//
+// How.  For a unit (sequence b, KV head g) the G query heads of all N nodes
+// share every key, so they are packed as the M rows of the MMA:
+// row r = node * G + head_in_group.  One CTA owns one tile of 128 rows and one
+// split of the unit's prefix (a run of 128-token KV tiles); the last split
+// also runs the tree block: the N tree keys, gated per row by the ancestry
+// bitmask.  All of these share one online softmax.
+//
+//   warps 0-3  softmax: thread t owns TMEM lane t = row t.  Loads S from TMEM,
+//              masks, tracks the running max/sum, writes P (bf16) back over S,
+//              rescales O when the max moves by more than 2^8 (exact: the final
+//              normalisation uses the same running max), writes the output.
+//   warp 4     producer: TMEM allocation; TMA loads of the Q tile and of the
+//              K/V tiles (paged blocks: one box per block) into a 3-stage ring.
+//   warp 5     MMA issuer (one thread): S = Q K^T (both operands in swizzled
+//              shared memory), O += P V (P read from TMEM, V from shared
+//              memory), in the order QK0, QK1, PV0, QK2, PV1, ... so that the
+//              next tile's QK^T runs while the softmax works on this one.
+//
+// TMEM (512 columns): O at [0, D), S buffers at [128, 256) and [256, 384).
+// Every mbarrier wait is bounded; a timeout sets a shared abort flag, every
+// role winds down, the CTA frees its TMEM and reports TS_ERR_TIMEOUT.
+#include "internal.cuh"
+#include "sm100.cuh"
+#include "tensor_map.cuh"
+
+namespace ts {
+namespace {
+
+using namespace sm100;
+
+constexpr int NUM_THREADS = 192;
+constexpr int SOFTMAX_THREADS = 128;
+constexpr int PRODUCER_WARP = 4;
+constexpr int MMA_WARP = 5;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_O = 0;
+constexpr uint32_t TMEM_S0 = 128;
+constexpr uint64_t WAIT_LIMIT_NS = 200000000ull;   // 200 ms: far above any legitimate wait
+constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units
+constexpr float NEG_INF = -INFINITY;
+
+template <int D>
+struct Cfg {
+  static constexpr int HALVES = D / 64;                        // 128-byte swizzle atoms along D
+  static constexpr int TILE_BYTES = KV_TILE * D * 2;           // one K or V tile
+  static constexpr int HALF_BYTES = KV_TILE * 128;             // one 64-column half of a tile
+  static constexpr int Q_BYTES = ROW_TILE * D * 2;
+  static constexpr int NST = (D == 128) ? 3 : 6;               // K/V ring depth
+};
+
+template <int D>
+struct __align__(1024) Smem {
+  uint8_t q[Cfg<D>::Q_BYTES];
+  uint8_t k[Cfg<D>::NST][Cfg<D>::TILE_BYTES];
+  uint8_t v[Cfg<D>::NST][Cfg<D>::TILE_BYTES];
+  uint64_t q_full;
+  uint64_t k_full[Cfg<D>::NST];
+  uint64_t v_full[Cfg<D>::NST];
+  uint64_t kv_empty[Cfg<D>::NST];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_ready;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct TcArgs {
+  AttnArgs a;
+  int box_rows;   // rows per paged TMA box: min(block_size, 128)
+  int direct;     // 1: a single split per unit -> write bf16 out (+ lse) directly
+};
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tm_q,
+          const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
+          const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const AttnArgs& a = args.a;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rt = blockIdx.x, split = blockIdx.y, unit = blockIdx.z;
+  const int b = unit / a.Hkv, g = unit - b * a.Hkv;
+
+  int P;
+  const bool p_ok = usable_prefix(a.prefix_len[b], a.chunk_tiles, a.max_splits, a.bs, a.max_blocks, &P);
+  const int tiles = prefix_tiles(P);
+  const int ns = num_splits(P, a.chunk_tiles);
+  if (split >= ns) return;  // whole CTA leaves before any barrier or TMEM use
+  if (!p_ok && threadIdx.x == 0 && rt == 0 && split == 0 && a.status) a.status[b] = TS_ERR_SHAPE;
+  const int t_begin = split * a.chunk_tiles;
+  const int n_prefix = min(tiles, t_begin + a.chunk_tiles) - t_begin;
+  const int n_tree = (split == ns - 1) ? ceil_div(a.N, KV_TILE) : 0;
+  const int n_tiles = n_prefix + n_tree;
+
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    mbar_init(&sm.q_full, 1);
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&sm.k_full[i], 1);
+      mbar_init(&sm.v_full[i], 1);
+      mbar_init(&sm.kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.p_full[i], SOFTMAX_THREADS);
+    }
+    mbar_init(&sm.o_ready, 1);
+    fence_barrier_init();
+  }
+  if (warp == PRODUCER_WARP) tmem_alloc(&sm.tmem_base, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_kc);
+      tma_prefetch_desc(&tm_vc);
+      tma_prefetch_desc(&tm_kt);
+      tma_prefetch_desc(&tm_vt);
+      mbar_arrive_expect_tx(&sm.q_full, C::Q_BYTES);
+      const int nodes_per_tile = ROW_TILE / a.G;
+      for (int h = 0; h < C::HALVES; ++h)
+        tma_load_4d(sm.q + h * (ROW_TILE * 128), &tm_q, &sm.q_full, 64 * h, g * a.G, rt * nodes_per_tile, b);
+    }
+    const int boxes = KV_TILE / args.box_rows;  // boxes per tile half (1 .. 8)
+    const uint32_t box_bytes = args.box_rows * 128;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int slot = j % C::NST;
+      if (j >= C::NST && !__all_sync(0xffffffffu, wait_bar(&sm.kv_empty[slot], ((j / C::NST) - 1) & 1, abort_flag)))
+        break;
+      if (j < n_prefix) {
+        const int key0 = (t_begin + j) * KV_TILE;
+        // lane i < boxes handles the box of tokens [key0 + i*box_rows, +box_rows)
+        int blk = 0, row0 = 0;
+        bool issue = false;
+        if (lane < boxes) {
+          const int t0 = key0 + lane * args.box_rows;
+          if (t0 < P) {
+            const int bi = t0 / a.bs;
+            blk = a.block_table[(size_t)b * a.max_blocks + bi];
+            if (blk < 0 || blk >= a.num_blocks) {
+              if (a.status) a.status[b] = TS_ERR_BAD_BLOCK;
+              blk = 0;  // read a valid block instead; the sequence is reported as failed
+            }
+            row0 = t0 - bi * a.bs;
+            issue = true;
+          }
+        }
+        const unsigned mask = __ballot_sync(0xffffffffu, issue);
+        const uint32_t bytes = __popc(mask) * box_bytes * C::HALVES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&sm.k_full[slot], bytes);
+          mbar_arrive_expect_tx(&sm.v_full[slot], bytes);
+        }
+        __syncwarp();
+        if (issue) {
+          const int z = blk * a.Hkv + g;
+          for (int h = 0; h < C::HALVES; ++h) {
+            uint8_t* kd = sm.k[slot] + h * C::HALF_BYTES + lane * box_bytes;
+            tma_load_3d(kd, &tm_kc, &sm.k_full[slot], 64 * h, row0, z);
+          }
+          for (int h = 0; h < C::HALVES; ++h) {
+            uint8_t* vd = sm.v[slot] + h * C::HALF_BYTES + lane * box_bytes;
+            tma_load_3d(vd, &tm_vc, &sm.v_full[slot], 64 * h, row0, z);
+          }
+        }
+      } else if (lane == 0) {
+        const int n0 = (j - n_prefix) * KV_TILE;  // first tree node of this tile; nodes >= N read as zeros
+        mbar_arrive_expect_tx(&sm.k_full[slot], C::TILE_BYTES);
+        mbar_arrive_expect_tx(&sm.v_full[slot], C::TILE_BYTES);
+        for (int h = 0; h < C::HALVES; ++h)
+          tma_load_4d(sm.k[slot] + h * C::HALF_BYTES, &tm_kt, &sm.k_full[slot], 64 * h, g, n0, b);
+        for (int h = 0; h < C::HALVES; ++h)
+          tma_load_4d(sm.v[slot] + h * C::HALF_BYTES, &tm_vt, &sm.v_full[slot], 64 * h, g, n0, b);
+      }
+      __syncwarp();
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_QK = idesc_bf16_f32(128, KV_TILE, 0, 0);
+      constexpr uint32_t ID_PV = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t q_addr = smem_u32(sm.q);
+      auto issue_qk = [&](int j) -> bool {
+        const int slot = j % C::NST;
+        if (!wait_bar(&sm.k_full[slot], (j / C::NST) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sm.k[slot]);
+        const uint32_t d_tmem = tmem + TMEM_S0 + (j & 1) * 128;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (ROW_TILE * 128) + (k & 3) * 32;
+          const uint32_t koff = (k >> 2) * C::HALF_BYTES + (k & 3) * 32;
+          mma_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + koff, 16, 1024), ID_QK,
+                 k > 0);
+        }
+        mma_commit(&sm.s_full[j & 1]);
+        return true;
+      };
+      bool ok = wait_bar(&sm.q_full, 0, abort_flag) && issue_qk(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles && !issue_qk(j + 1)) break;
+        const int slot = j % C::NST;
+        if (!wait_bar(&sm.p_full[j & 1], (j >> 1) & 1, abort_flag)) break;
+        if (!wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sm.v[slot]);
+        const uint32_t p_tmem = tmem + TMEM_S0 + (j & 1) * 128;
+#pragma unroll
+        for (int k = 0; k < KV_TILE / 16; ++k)
+          mma_ts(tmem + TMEM_O, p_tmem + k * 8, smem_desc_sw128(v_addr + k * 2048, C::HALF_BYTES, 1024), ID_PV,
+                 j > 0 || k > 0);
+        mma_commit(&sm.o_ready);
+        mma_commit(&sm.kv_empty[slot]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r = threadIdx.x;  // TMEM lane == packed row within the tile
+    const int R = a.N * a.G;
+    const int grow = rt * ROW_TILE + r;
+    const bool active = grow < R;
+    const int node = active ? grow / a.G : 0;
+    const int h = g * a.G + (active ? grow - node * a.G : 0);
+    // ancestry words of this row; words past W stay zero.  Padding rows (past
+    // N*G) see every key so that their softmax stays finite; never written out.
+    uint64_t anc[4] = {0ull, 0ull, 0ull, 0ull};
+    if (active) {
+      for (int w = 0; w < a.W; ++w) anc[w] = a.anc_mask[((size_t)b * a.N + node) * a.W + w];
+    } else {
+      anc[0] = anc[1] = anc[2] = anc[3] = ~0ull;
+    }
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m_run = NEG_INF, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      if (!__all_sync(0xffffffffu, wait_bar(&sm.s_full[j & 1], (j >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t s_tmem = tmem + lane_base + TMEM_S0 + (j & 1) * 128;
+      float s[KV_TILE];
+#pragma unroll
+      for (int c = 0; c < KV_TILE / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(s_tmem + c * 32, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(u[e]);
+      }
+      // masking: ragged prefix tail, or the tree block's ancestry bits
+      bool tail_zero_v = false;
+      int valid = KV_TILE;
+      if (j < n_prefix) {
+        const int key0 = (t_begin + j) * KV_TILE;
+        valid = min(KV_TILE, P - key0);
+        if (valid < KV_TILE) {
+          tail_zero_v = true;
+#pragma unroll
+          for (int c = 0; c < KV_TILE; ++c)
+            if (c >= valid) s[c] = NEG_INF;
+        }
+      } else {
+        const int tt = j - n_prefix;  // tree tile: nodes [128*tt, 128*tt + 128)
+        const uint64_t lo = tt == 0 ? anc[0] : (tt == 1 ? anc[2] : 0ull);
+        const uint64_t hi = tt == 0 ? anc[1] : (tt == 1 ? anc[3] : 0ull);
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (!((lo >> c) & 1ull)) s[c] = NEG_INF;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (!((hi >> c) & 1ull)) s[64 + c] = NEG_INF;
+      }
+      float mx = NEG_INF;
+#pragma unroll
+      for (int c = 0; c < KV_TILE; ++c) mx = fmaxf(mx, s[c]);
+      mx *= a.scale_log2;
+      const float m_new = fmaxf(m_run, mx);
+      const bool rescale = (j > 0) && (m_new > m_run + RESCALE_THRESHOLD);
+      float m_use = m_run;
+      if (j == 0 || rescale) m_use = m_new;
+      // nothing visible so far: every p is 0 (and O is rescaled away later)
+      const float m_exp = (m_use == NEG_INF) ? 0.f : m_use;
+      // p = 2^(s*scale*log2e - m), packed to bf16 pairs and written over S
+      float rowsum = 0.f;
+      uint32_t pk[KV_TILE / 2];
+#pragma unroll
+      for (int c = 0; c < KV_TILE; c += 2) {
+        const float p0 = ex2(fmaf(s[c], a.scale_log2, -m_exp));
+        const float p1 = ex2(fmaf(s[c + 1], a.scale_log2, -m_exp));
+        rowsum += p0 + p1;
+        pk[c / 2] = pack_bf16x2(p0, p1);
+      }
+      {
+        uint32_t part[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) part[e] = pk[e];
+        tmem_st32(s_tmem, part);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) part[e] = pk[32 + e];
+        tmem_st32(s_tmem + 32, part);
+      }
+      if (tail_zero_v) {
+        // rows >= valid of this V tile hold whatever the pool had past the
+        // prefix (or stale data): zero them so 0 * V can never be NaN
+        const int slot = j % C::NST;
+        if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        if (r >= valid) {
+          for (int hh = 0; hh < C::HALVES; ++hh) {
+            uint4* row = reinterpret_cast<uint4*>(sm.v[slot] + hh * C::HALF_BYTES + r * 128);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      if (j > 0) {
+        // O holds PV_{j-1} once it completes; needed before a rescale (and it
+        // keeps the o_ready phases consumed in order)
+        if (!__all_sync(0xffffffffu, wait_bar(&sm.o_ready, (j - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // TMEM loads/stores are warp-collective: the whole warp rescales its
+        // rows together, with factor 1 for rows whose max did not move enough
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = !rescale ? 1.f : ((m_run == NEG_INF) ? 0.f : ex2(m_run - m_new));
+          l_run *= f;
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_base + TMEM_O + c, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
+            tmem_st32(tmem + lane_base + TMEM_O + c, u);
+          }
+        }
+      }
+      m_run = m_use;
+      l_run += rowsum;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[j & 1]);
+    }
+    // epilogue: wait for the last PV, normalise, write
+    if (ok && __all_sync(0xffffffffu, wait_bar(&sm.o_ready, (n_tiles - 1) & 1, abort_flag))) {
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      const float lse2 = m_run + __log2f(l_run);
+      const size_t orow = ((size_t)b * a.N + node) * a.Hq + h;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_base + TMEM_O + c, u);
+        tmem_ld_wait();
+        if (active) {
+          if (args.direct) {
+            uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + c);
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(u[e + 0]) * inv, __uint_as_float(u[e + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(u[e + 2]) * inv, __uint_as_float(u[e + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(u[e + 4]) * inv, __uint_as_float(u[e + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(u[e + 6]) * inv, __uint_as_float(u[e + 7]) * inv);
+              dst[e / 8] = v;
+            }
+          } else {
+            const size_t rows = (size_t)a.B * a.N * a.Hq;
+            float4* dst = reinterpret_cast<float4*>(a.part_o + (size_t)split * rows * D + orow * D + c);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              dst[e / 4] = make_float4(__uint_as_float(u[e]) * inv, __uint_as_float(u[e + 1]) * inv,
+                                       __uint_as_float(u[e + 2]) * inv, __uint_as_float(u[e + 3]) * inv);
+          }
+        }
+      }
+      if (active) {
+        if (args.direct) {
+          if (a.lse) a.lse[orow] = lse2 * 0.69314718055994531f;
+        } else {
+          a.part_lse[(size_t)split * ((size_t)a.B * a.N * a.Hq) + orow] = lse2;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (sm.abort_flag && threadIdx.x == 0 && a.status) a.status[b] = TS_ERR_TIMEOUT;
+  if (warp == PRODUCER_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int D>
+constexpr size_t smem_bytes() {
+  return sizeof(Smem<D>) + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+}
+
+template <int D>
+cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
+  TcArgs t{};
+  t.a = a;
+  t.box_rows = a.bs < KV_TILE ? a.bs : KV_TILE;
+  t.direct = a.max_splits == 1;
+  CUtensorMap m_q, m_kc, m_vc, m_kt, m_vt;
+  // q [B, N, Hq, D]: dims (D, Hq, N, B); box (64, G, 128/G, 1) = 128 packed rows
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.N, (uint64_t)a.B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)a.Hq * D * 2, (uint64_t)a.N * a.Hq * D * 2};
+    const uint32_t box[4] = {64, (uint32_t)a.G, (uint32_t)(ROW_TILE / a.G), 1};
+    if (!encode_bf16_sw128(&m_q, a.q, 4, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  // KV pool [num_blocks, Hkv, bs, D]: dims (D, bs, num_blocks*Hkv); box (64, box_rows, 1)
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.bs, (uint64_t)a.num_blocks * a.Hkv};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)a.bs * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)t.box_rows, 1};
+    if (!encode_bf16_sw128(&m_kc, a.k_cache, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_bf16_sw128(&m_vc, a.v_cache, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  // tree K/V [B, N, Hkv, D]: dims (D, Hkv, N, B); box (64, 1, 128, 1); nodes >= N read as zeros
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hkv, (uint64_t)a.N, (uint64_t)a.B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)a.Hkv * D * 2, (uint64_t)a.N * a.Hkv * D * 2};
+    const uint32_t box[4] = {64, 1, (uint32_t)KV_TILE, 1};
+    if (!encode_bf16_sw128(&m_kt, a.k_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_bf16_sw128(&m_vt, a.v_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  dim3 grid(a.row_tiles, a.max_splits, a.B * a.Hkv);
+  k_attn_tc<D><<<grid, NUM_THREADS, smem_bytes<D>(), s>>>(t, m_q, m_kc, m_vc, m_kt, m_vt);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t attn_tc_prepare() {
+  // per-process opt-in to the large shared-memory carve-out (not a stream
+  // operation; done outside any capture by the first call)
+  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bytes<128>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_attn_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<64>());
+}
+
+cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s) {
+  return a.D == 128 ? launch_tc<128>(a, s) : launch_tc<64>(a, s);
+}
+
+}  // namespace ts

@@ -80,7 +80,8 @@ struct AttnPlan {
 cudaError_t launch_ancestry(const int32_t* parent, const int32_t* prefix_len, int B, int N,
                             uint64_t* anc, int32_t* depth, int32_t* pos, int32_t* status,
                             cudaStream_t s);
-cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+cudaError_t attn_tc_prepare();
+cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s);
 
 struct VerifyArgs {
