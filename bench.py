@@ -270,11 +270,12 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    base = W.make(args.workload)
+    base = W.make(args.workload, **workload_overrides(args))
     set_bytes = sum(x.nbytes for x in (base.q, base.k_cache, base.v_cache, base.k_tree, base.v_tree)) + \
         (base.logits.nbytes if base.logits is not None else 0)
     nsets = max(1, min(16, math.ceil(2 * L2_BYTES / set_bytes))) if set_bytes < 2 * L2_BYTES else 1
-    cases = [base] + [W.make(args.workload, seed=20270000 + 97 * k) for k in range(1, nsets)]
+    cases = [base] + [W.make(args.workload, seed=20270000 + 97 * k, **workload_overrides(args))
+                      for k in range(1, nsets)]
     dsets = [to_dev(c, dev) for c in cases]
     # one set of output buffers per input set (prefix lengths, hence the split plan, may differ)
     steps = [TreeVerifyStep(c.B, c.N, c.Hq, c.Hkv, c.D, c.prefix_len, vocab=c.vocab, max_depth=c.N - 1,
@@ -493,7 +494,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     import workloads as W
-    case = W.make(args.workload)
+    case = W.make(args.workload, **workload_overrides(args))
     for _ in range(max(0, min(args.warmup, 1))):
         oracle_sample_step(case)
     w0 = time.time()
@@ -512,6 +513,19 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def workload_overrides(args) -> dict:
+    kw = {}
+    if args.batch:
+        if args.workload != "c4":
+            raise SystemExit("--batch applies to c4 only")
+        kw["batch"] = args.batch
+    if args.prefix:
+        if args.workload != "c5":
+            raise SystemExit("--prefix applies to c5 only")
+        kw["prefix"] = args.prefix
+    return kw
+
+
 def default_steps(workload: str) -> int:
     return {"c1": 20000, "c2": 20000, "c3": 2000, "c4": 200, "c5": 200}[workload]
 
@@ -525,6 +539,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="c2")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch of c4 (smaller profiling case)")
+    ap.add_argument("--prefix", type=int, default=0, help="override the prefix length of c5")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -42,34 +42,59 @@ ts_status check_attn(const ts_attn_params* p) {
   return TS_OK;
 }
 
-// Split plan: cut every unit's prefix into equal chunks of tiles so that the
-// grid holds about two CTAs per SM across all units and row tiles.
+// Split plan.  Every (unit, row tile) is one chain of 128-token KV tiles; a
+// split cuts the chain into CTAs of `chunk_tiles` tiles (the last one of a
+// unit also runs the tree block).  The attention kernel holds one CTA per SM,
+// so the time of a plan is about
+//     waves * (chunk + per-CTA overhead) + cost of the split partials,
+// in units of one tile's work on one SM (about 0.5 us).  The partials are
+// written and read back once (fp32 O + lse per split), priced at the
+// measured HBM rate.  The plan with the smallest estimate wins.
 AttnPlan plan_attn(const ts_attn_params* p) {
   AttnPlan pl{};
   const int G = p->Hq / p->Hkv;
   pl.row_tiles = ceil_div(p->N * G, ROW_TILE);
-  long long total = 0;
-  int max_tiles = 0;
+  const int tree_tiles = ceil_div(p->N, KV_TILE);
+  int max_tiles = 1;
   for (int b = 0; b < p->B; ++b) {
     const int t = prefix_tiles(p->prefix_len_host[b]);
-    total += t;
     max_tiles = t > max_tiles ? t : max_tiles;
   }
-  total *= (long long)p->Hkv * pl.row_tiles;
-  const long long target = 2LL * PLAN_SMS;
-  long long chunk = (total + target - 1) / target;
-  if (chunk < 1) chunk = 1;
-  pl.chunk_tiles = (int)chunk;
+  const double rows = (double)p->B * p->N * p->Hq;
+  const double tile_bytes_equiv = 3.6e6;  // HBM bytes moved in one tile-time
+  const double cta_overhead = 1.5;        // prologue + epilogue, in tile-times
+  double best = 1e300;
+  int best_chunk = max_tiles;
+  for (int s = 1; s <= 256; ++s) {
+    const int chunk = ceil_div(max_tiles, s);
+    if (s > 1 && chunk == ceil_div(max_tiles, s - 1)) continue;
+    long long ctas = 0;
+    int splits = 1;
+    for (int b = 0; b < p->B; ++b) {
+      const int ns = num_splits(p->prefix_len_host[b], chunk);
+      ctas += (long long)ns * p->Hkv * pl.row_tiles;
+      splits = ns > splits ? ns : splits;
+    }
+    const double waves = (double)((ctas + PLAN_SMS - 1) / PLAN_SMS);
+    double cost = waves * (chunk + cta_overhead) + tree_tiles;
+    if (splits > 1) cost += 2.0 * splits * rows * (p->D + 1) * 4.0 / tile_bytes_equiv;
+    if (cost < best) {
+      best = cost;
+      best_chunk = chunk;
+    }
+    if (chunk == 1) break;
+  }
+  pl.chunk_tiles = best_chunk;
   pl.max_splits = 1;
   for (int b = 0; b < p->B; ++b) {
     const int ns = num_splits(p->prefix_len_host[b], pl.chunk_tiles);
     pl.max_splits = ns > pl.max_splits ? ns : pl.max_splits;
   }
-  const size_t rows = (size_t)p->B * p->N * p->Hq;
-  pl.part_o_bytes = round256((size_t)pl.max_splits * rows * p->D * sizeof(float));
-  pl.part_lse_bytes = round256((size_t)pl.max_splits * rows * sizeof(float));
+  const size_t nrows = (size_t)p->B * p->N * p->Hq;
+  pl.part_o_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * p->D * sizeof(float)) : 0;
+  pl.part_lse_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * sizeof(float)) : 0;
   pl.workspace_bytes = pl.part_o_bytes + pl.part_lse_bytes;
-  (void)max_tiles;
+  if (pl.workspace_bytes == 0) pl.workspace_bytes = 256;  // keep a non-empty workspace contract
   return pl;
 }
 

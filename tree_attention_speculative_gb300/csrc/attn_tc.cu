@@ -23,6 +23,9 @@
 //              memory), in the order QK0, QK1, PV0, QK2, PV1, ... so that the
 //              next tile's QK^T runs while the softmax works on this one.
 //
+// Shared-memory K/V tiles of the prefix are laid out [8-row group][D half]
+// [8 rows x 128 B] (each 1 KB piece one 128-byte-swizzle atom), so one TMA box
+// brings every D column of a paged block; tree tiles are [D half][128 rows].
 // TMEM (512 columns): O at [0, D), S buffers at [128, 256) and [256, 384).
 // Every mbarrier wait is bounded; a timeout sets a shared abort flag, every
 // role winds down, the CTA frees its TMEM and reports TS_ERR_TIMEOUT.
@@ -157,47 +160,55 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       for (int h = 0; h < C::HALVES; ++h)
         tma_load_4d(sm.q + h * (ROW_TILE * 128), &tm_q, &sm.q_full, 64 * h, g * a.G, rt * nodes_per_tile, b);
     }
-    const int boxes = KV_TILE / args.box_rows;  // boxes per tile half (1 .. 8)
-    const uint32_t box_bytes = args.box_rows * 128;
+    const int boxes = KV_TILE / args.box_rows;  // boxes (paged blocks) per tile (1 .. 8)
+    const uint32_t box_bytes = args.box_rows * D * 2;
+    // Block-table entries are software-pipelined: lane L holds the entry of
+    // box (L % boxes) of tile (L / boxes) of a group of 32/boxes tiles; the
+    // next group is loaded (one coalesced read) when the current one starts,
+    // so the table's load latency hides behind several tiles of TMA issue.
+    const int tpg = 32 / boxes;
+    const int* table_row = a.block_table + (size_t)b * a.max_blocks;
+    auto load_group = [&](int grp) -> int {
+      const int tile = grp * tpg + lane / boxes;
+      const int t0 = (t_begin + tile) * KV_TILE + (lane % boxes) * args.box_rows;
+      if (tile >= n_prefix || t0 >= P) return 0;
+      int blk = table_row[t0 / a.bs];
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (a.status) a.status[b] = TS_ERR_BAD_BLOCK;
+        blk = 0;  // read a valid block instead; the sequence is reported as failed
+      }
+      return blk;
+    };
+    int grp_cur = load_group(0);
+    int grp_nxt = (n_prefix > tpg) ? load_group(1) : 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int slot = j % C::NST;
       if (j >= C::NST && !__all_sync(0xffffffffu, wait_bar(&sm.kv_empty[slot], ((j / C::NST) - 1) & 1, abort_flag)))
         break;
       if (j < n_prefix) {
+        if (j > 0 && j % tpg == 0) {
+          grp_cur = grp_nxt;
+          const int g2 = j / tpg + 1;
+          grp_nxt = (g2 * tpg < n_prefix) ? load_group(g2) : 0;
+        }
         const int key0 = (t_begin + j) * KV_TILE;
         // lane i < boxes handles the box of tokens [key0 + i*box_rows, +box_rows)
-        int blk = 0, row0 = 0;
-        bool issue = false;
-        if (lane < boxes) {
-          const int t0 = key0 + lane * args.box_rows;
-          if (t0 < P) {
-            const int bi = t0 / a.bs;
-            blk = a.block_table[(size_t)b * a.max_blocks + bi];
-            if (blk < 0 || blk >= a.num_blocks) {
-              if (a.status) a.status[b] = TS_ERR_BAD_BLOCK;
-              blk = 0;  // read a valid block instead; the sequence is reported as failed
-            }
-            row0 = t0 - bi * a.bs;
-            issue = true;
-          }
-        }
+        const int blk = __shfl_sync(0xffffffffu, grp_cur, ((j % tpg) * boxes + lane) & 31);
+        const int t0 = key0 + lane * args.box_rows;
+        const bool issue = lane < boxes && t0 < P;
+        const int row0 = t0 % a.bs;
         const unsigned mask = __ballot_sync(0xffffffffu, issue);
-        const uint32_t bytes = __popc(mask) * box_bytes * C::HALVES;
+        const uint32_t bytes = __popc(mask) * box_bytes;
         if (lane == 0) {
           mbar_arrive_expect_tx(&sm.k_full[slot], bytes);
           mbar_arrive_expect_tx(&sm.v_full[slot], bytes);
         }
         __syncwarp();
         if (issue) {
+          // one box = every D column of box_rows tokens of one paged block
           const int z = blk * a.Hkv + g;
-          for (int h = 0; h < C::HALVES; ++h) {
-            uint8_t* kd = sm.k[slot] + h * C::HALF_BYTES + lane * box_bytes;
-            tma_load_3d(kd, &tm_kc, &sm.k_full[slot], 64 * h, row0, z);
-          }
-          for (int h = 0; h < C::HALVES; ++h) {
-            uint8_t* vd = sm.v[slot] + h * C::HALF_BYTES + lane * box_bytes;
-            tma_load_3d(vd, &tm_vc, &sm.v_full[slot], 64 * h, row0, z);
-          }
+          tma_load_5d(sm.k[slot] + lane * box_bytes, &tm_kc, &sm.k_full[slot], 0, 0, 0, row0 >> 3, z);
+          tma_load_5d(sm.v[slot] + lane * box_bytes, &tm_vc, &sm.v_full[slot], 0, 0, 0, row0 >> 3, z);
         }
       } else if (lane == 0) {
         const int n0 = (j - n_prefix) * KV_TILE;  // first tree node of this tile; nodes >= N read as zeros
@@ -222,11 +233,16 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm.k[slot]);
         const uint32_t d_tmem = tmem + TMEM_S0 + (j & 1) * 128;
+        // prefix tiles: D halves 1 KB apart, 8-row groups HALVES KB apart;
+        // tree tiles: D halves 16 KB apart, 8-row groups 1 KB apart
+        const bool tree = j >= n_prefix;
+        const uint32_t k_half = tree ? C::HALF_BYTES : 1024;
+        const uint32_t k_sbo = tree ? 1024 : C::HALVES * 1024;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (ROW_TILE * 128) + (k & 3) * 32;
-          const uint32_t koff = (k >> 2) * C::HALF_BYTES + (k & 3) * 32;
-          mma_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + koff, 16, 1024), ID_QK,
+          const uint32_t koff = (k >> 2) * k_half + (k & 3) * 32;
+          mma_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + koff, 16, k_sbo), ID_QK,
                  k > 0);
         }
         mma_commit(&sm.s_full[j & 1]);
@@ -241,9 +257,12 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sm.v[slot]);
         const uint32_t p_tmem = tmem + TMEM_S0 + (j & 1) * 128;
+        const bool tree = j >= n_prefix;
+        const uint32_t v_lbo = tree ? C::HALF_BYTES : 1024;           // between D halves
+        const uint32_t v_sbo = tree ? 1024 : C::HALVES * 1024;         // between 8-key groups
 #pragma unroll
         for (int k = 0; k < KV_TILE / 16; ++k)
-          mma_ts(tmem + TMEM_O, p_tmem + k * 8, smem_desc_sw128(v_addr + k * 2048, C::HALF_BYTES, 1024), ID_PV,
+          mma_ts(tmem + TMEM_O, p_tmem + k * 8, smem_desc_sw128(v_addr + k * 2 * v_sbo, v_lbo, v_sbo), ID_PV,
                  j > 0 || k > 0);
         mma_commit(&sm.o_ready);
         mma_commit(&sm.kv_empty[slot]);
@@ -276,13 +295,18 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       tc_fence_after();
       const uint32_t s_tmem = tmem + lane_base + TMEM_S0 + (j & 1) * 128;
       float s[KV_TILE];
+      {
+        // all four TMEM loads in flight before one wait
+        uint32_t u[KV_TILE / 32][32];
 #pragma unroll
-      for (int c = 0; c < KV_TILE / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(s_tmem + c * 32, u);
+        for (int c = 0; c < KV_TILE / 32; ++c) tmem_ld32(s_tmem + c * 32, u[c]);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(u[e]);
+        for (int c = 0; c < KV_TILE / 32; ++c) {
+          reg_fence32(u[c]);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(u[c][e]);
+        }
       }
       // masking: ragged prefix tail, or the tree block's ancestry bits
       bool tail_zero_v = false;
@@ -307,9 +331,15 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         for (int c = 0; c < 64; ++c)
           if (!((hi >> c) & 1ull)) s[64 + c] = NEG_INF;
       }
-      float mx = NEG_INF;
+      // row max with 8 independent chains, then a 3-level tree
+      float mk[8];
 #pragma unroll
-      for (int c = 0; c < KV_TILE; ++c) mx = fmaxf(mx, s[c]);
+      for (int e = 0; e < 8; ++e) mk[e] = s[e];
+#pragma unroll
+      for (int c = 8; c < KV_TILE; c += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mk[e] = fmaxf(mk[e], s[c + e]);
+      float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
       mx *= a.scale_log2;
       const float m_new = fmaxf(m_run, mx);
       const bool rescale = (j > 0) && (m_new > m_run + RESCALE_THRESHOLD);
@@ -318,15 +348,16 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       // nothing visible so far: every p is 0 (and O is rescaled away later)
       const float m_exp = (m_use == NEG_INF) ? 0.f : m_use;
       // p = 2^(s*scale*log2e - m), packed to bf16 pairs and written over S
-      float rowsum = 0.f;
+      float sk[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial sums
       uint32_t pk[KV_TILE / 2];
 #pragma unroll
       for (int c = 0; c < KV_TILE; c += 2) {
         const float p0 = ex2(fmaf(s[c], a.scale_log2, -m_exp));
         const float p1 = ex2(fmaf(s[c + 1], a.scale_log2, -m_exp));
-        rowsum += p0 + p1;
+        sk[(c >> 1) & 3] += p0 + p1;
         pk[c / 2] = pack_bf16x2(p0, p1);
       }
+      const float rowsum = (sk[0] + sk[1]) + (sk[2] + sk[3]);
       {
         uint32_t part[32];
 #pragma unroll
@@ -346,7 +377,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         }
         if (r >= valid) {
           for (int hh = 0; hh < C::HALVES; ++hh) {
-            uint4* row = reinterpret_cast<uint4*>(sm.v[slot] + hh * C::HALF_BYTES + r * 128);
+            uint4* row = reinterpret_cast<uint4*>(sm.v[slot] + ((r >> 3) * C::HALVES + hh) * 1024 + (r & 7) * 128);
 #pragma unroll
             for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
           }
@@ -367,13 +398,19 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
           const float f = !rescale ? 1.f : ((m_run == NEG_INF) ? 0.f : ex2(m_run - m_new));
           l_run *= f;
 #pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t u[32];
-            tmem_ld32(tmem + lane_base + TMEM_O + c, u);
+          for (int c = 0; c < D; c += 64) {
+            uint32_t u0[32], u1[32];
+            tmem_ld32(tmem + lane_base + TMEM_O + c, u0);
+            if (c + 32 < D) tmem_ld32(tmem + lane_base + TMEM_O + c + 32, u1);
             tmem_ld_wait();
+            reg_fence32(u0);
+            reg_fence32(u1);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
-            tmem_st32(tmem + lane_base + TMEM_O + c, u);
+            for (int e = 0; e < 32; ++e) u0[e] = __float_as_uint(__uint_as_float(u0[e]) * f);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u1[e] = __float_as_uint(__uint_as_float(u1[e]) * f);
+            tmem_st32(tmem + lane_base + TMEM_O + c, u0);
+            if (c + 32 < D) tmem_st32(tmem + lane_base + TMEM_O + c + 32, u1);
           }
         }
       }
@@ -454,13 +491,15 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
     const uint32_t box[4] = {64, (uint32_t)a.G, (uint32_t)(ROW_TILE / a.G), 1};
     if (!encode_bf16_sw128(&m_q, a.q, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
-  // KV pool [num_blocks, Hkv, bs, D]: dims (D, bs, num_blocks*Hkv); box (64, box_rows, 1)
+  // KV pool [num_blocks, Hkv, bs, D] viewed as (64 columns, 8 rows, D/64 halves,
+  // bs/8 row groups, num_blocks*Hkv slabs): a box (64, 8, D/64, box_rows/8, 1)
+  // lands in shared memory as [row group][half][8 rows x 128 B]
   {
-    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.bs, (uint64_t)a.num_blocks * a.Hkv};
-    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)a.bs * D * 2};
-    const uint32_t box[3] = {64, (uint32_t)t.box_rows, 1};
-    if (!encode_bf16_sw128(&m_kc, a.k_cache, 3, dims, str, box)) return cudaErrorInvalidValue;
-    if (!encode_bf16_sw128(&m_vc, a.v_cache, 3, dims, str, box)) return cudaErrorInvalidValue;
+    const uint64_t dims[5] = {64, 8, (uint64_t)(D / 64), (uint64_t)(a.bs / 8), (uint64_t)a.num_blocks * a.Hkv};
+    const uint64_t str[4] = {(uint64_t)D * 2, 128, (uint64_t)8 * D * 2, (uint64_t)a.bs * D * 2};
+    const uint32_t box[5] = {64, 8, (uint32_t)(D / 64), (uint32_t)(t.box_rows / 8), 1};
+    if (!encode_bf16_sw128(&m_kc, a.k_cache, 5, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_bf16_sw128(&m_vc, a.v_cache, 5, dims, str, box)) return cudaErrorInvalidValue;
   }
   // tree K/V [B, N, Hkv, D]: dims (D, Hkv, N, B); box (64, 1, 128, 1); nodes >= N read as zeros
   {
