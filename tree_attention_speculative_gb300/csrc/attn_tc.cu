@@ -18,10 +18,15 @@
 //              normalisation uses the same running max), writes the output.
 //   warp 4     producer: TMEM allocation; TMA loads of the Q tile and of the
 //              K/V tiles (paged blocks: one box per block) into a 3-stage ring.
-//   warp 5     MMA issuer (one thread): S = Q K^T (both operands in swizzled
-//              shared memory), O += P V (P read from TMEM, V from shared
-//              memory), in the order QK0, QK1, PV0, QK2, PV1, ... so that the
-//              next tile's QK^T runs while the softmax works on this one.
+//   warp 5     QK issuer (one thread): S(j) = Q K(j)^T, both operands in
+//              swizzled shared memory, into S buffer j%2 once PV(j-2) (the
+//              last reader of that buffer) has completed (s_free[j%2]).
+//   warp 6     PV issuer (one thread): O += P(j) V(j), P read from TMEM, V
+//              from shared memory, as soon as the softmax has written P(j).
+//   One thread issues a tcgen05.mma only every ~120-160 cycles, about half
+//   the tensor pipe's rate for 128x128x16 instructions; with QK and PV on two
+//   issuers the next tile's QK^T and this tile's PV run while the softmax
+//   works, and the pipe sees both streams at once.
 //
 // Shared-memory K/V tiles of the prefix are laid out [8-row group][D half]
 // [8 rows x 128 B] (each 1 KB piece one 128-byte-swizzle atom), so one TMA box
@@ -38,10 +43,11 @@ namespace {
 
 using namespace sm100;
 
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;
 constexpr int SOFTMAX_THREADS = 128;
 constexpr int PRODUCER_WARP = 4;
-constexpr int MMA_WARP = 5;
+constexpr int QK_WARP = 5;
+constexpr int PV_WARP = 6;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_O = 0;
 constexpr uint32_t TMEM_S0 = 128;
@@ -69,6 +75,7 @@ struct __align__(1024) Smem {
   uint64_t kv_empty[Cfg<D>::NST];
   uint64_t s_full[2];
   uint64_t p_full[2];
+  uint64_t s_free[2];  // S buffer b no longer read: PV of its last tile completed
   uint64_t o_ready;
   uint32_t tmem_base;
   int abort_flag;
@@ -132,11 +139,12 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.v_full[i], 1);
-      mbar_init(&sm.kv_empty[i], 1);
+      mbar_init(&sm.kv_empty[i], 2);  // released by the QK and the PV issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.p_full[i], SOFTMAX_THREADS);
+      mbar_init(&sm.s_free[i], 1);
     }
     mbar_init(&sm.o_ready, 1);
     fence_barrier_init();
@@ -221,15 +229,19 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       }
       __syncwarp();
     }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == QK_WARP) {
+    // ------------------------------------------------------------ QK issuer
     if (lane == 0) {
       constexpr uint32_t ID_QK = idesc_bf16_f32(128, KV_TILE, 0, 0);
-      constexpr uint32_t ID_PV = idesc_bf16_f32(128, D, 0, 1);
       const uint32_t q_addr = smem_u32(sm.q);
-      auto issue_qk = [&](int j) -> bool {
+      bool ok = wait_bar(&sm.q_full, 0, abort_flag);
+      for (int j = 0; ok && j < n_tiles; ++j) {
         const int slot = j % C::NST;
-        if (!wait_bar(&sm.k_full[slot], (j / C::NST) & 1, abort_flag)) return false;
+        // K(j) has landed; S buffer j%2 is free once PV(j-2) has completed
+        // (a per-buffer barrier: it can never run two completions ahead)
+        ok = wait_bar(&sm.k_full[slot], (j / C::NST) & 1, abort_flag) &&
+             (j < 2 || wait_bar(&sm.s_free[j & 1], ((j >> 1) - 1) & 1, abort_flag));
+        if (!ok) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm.k[slot]);
         const uint32_t d_tmem = tmem + TMEM_S0 + (j & 1) * 128;
@@ -246,11 +258,14 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
                  k > 0);
         }
         mma_commit(&sm.s_full[j & 1]);
-        return true;
-      };
-      bool ok = wait_bar(&sm.q_full, 0, abort_flag) && issue_qk(0);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles && !issue_qk(j + 1)) break;
+        mma_commit(&sm.kv_empty[slot]);  // K(j) no longer read
+      }
+    }
+  } else if (warp == PV_WARP) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_PV = idesc_bf16_f32(128, D, 0, 1);
+      for (int j = 0; j < n_tiles; ++j) {
         const int slot = j % C::NST;
         if (!wait_bar(&sm.p_full[j & 1], (j >> 1) & 1, abort_flag)) break;
         if (!wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag)) break;
@@ -258,14 +273,15 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         const uint32_t v_addr = smem_u32(sm.v[slot]);
         const uint32_t p_tmem = tmem + TMEM_S0 + (j & 1) * 128;
         const bool tree = j >= n_prefix;
-        const uint32_t v_lbo = tree ? C::HALF_BYTES : 1024;           // between D halves
-        const uint32_t v_sbo = tree ? 1024 : C::HALVES * 1024;         // between 8-key groups
+        const uint32_t v_lbo = tree ? C::HALF_BYTES : 1024;    // between D halves
+        const uint32_t v_sbo = tree ? 1024 : C::HALVES * 1024;  // between 8-key groups
 #pragma unroll
         for (int k = 0; k < KV_TILE / 16; ++k)
           mma_ts(tmem + TMEM_O, p_tmem + k * 8, smem_desc_sw128(v_addr + k * 2 * v_sbo, v_lbo, v_sbo), ID_PV,
                  j > 0 || k > 0);
         mma_commit(&sm.o_ready);
-        mma_commit(&sm.kv_empty[slot]);
+        mma_commit(&sm.s_free[j & 1]);
+        mma_commit(&sm.kv_empty[slot]);  // V(j) no longer read
       }
     }
   } else {

@@ -27,22 +27,43 @@ k_combine(AttnArgs a) {
   const size_t stride_lse = (size_t)rows;
   const size_t stride_o = (size_t)rows * D;
 
+  // every split's lse in flight at once: lane s holds split s (then s+32, ...)
   float m = -INFINITY;
-  for (int s = 0; s < ns; ++s) m = fmaxf(m, a.part_lse[s * stride_lse + row]);
+  for (int s = lane; s < ns; s += 32) m = fmaxf(m, a.part_lse[s * stride_lse + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float acc[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) acc[k] = 0.f;
   float den = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float w = exp2f(a.part_lse[s * stride_lse + row] - m);
-    den += w;
-    const float* o = a.part_o + s * stride_o + (size_t)row * D + lane * PER;
-    if constexpr (PER == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(o);
-      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(o);
-      acc[0] += w * v.x; acc[1] += w * v.y;
+  // partial rows: up to 8 independent loads in flight per lane
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float w[8];
+    float v[8][PER];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int s = s0 + i;
+      w[i] = 0.f;
+      if (s < ns) {
+        w[i] = a.part_lse[s * stride_lse + row];
+        const float* o = a.part_o + s * stride_o + (size_t)row * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(o);
+          v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(o);
+          v[i][0] = x.x; v[i][1] = x.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (s0 + i < ns) {
+        const float wi = exp2f(w[i] - m);
+        den += wi;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) acc[k] = fmaf(wi, v[i][k], acc[k]);
+      }
     }
   }
   const float inv = 1.f / den;
