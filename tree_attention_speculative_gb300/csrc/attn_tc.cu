@@ -34,6 +34,7 @@
 // TMEM (512 columns): O at [0, D), S buffers at [128, 256) and [256, 384).
 // Every mbarrier wait is bounded; a timeout sets a shared abort flag, every
 // role winds down, the CTA frees its TMEM and reports TS_ERR_TIMEOUT.
+#include "fastexp.cuh"
 #include "internal.cuh"
 #include "sm100.cuh"
 #include "tensor_map.cuh"
@@ -79,6 +80,7 @@ struct __align__(1024) Smem {
   uint64_t o_ready;
   uint32_t tmem_base;
   int abort_flag;
+  int pv_done;  // PVs completed so far, published by the PV issuer (release/acquire)
 };
 
 struct TcArgs {
@@ -93,6 +95,26 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Bounded wait until the published PV count reaches `target`.
+__device__ __forceinline__ bool wait_count(const int* counter, int target, volatile int* abort_flag) {
+  const uint32_t addr = smem_u32(counter);
+  auto load = [&]() {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+  };
+  if (load() >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (load() >= target) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
       *abort_flag = 1;
@@ -135,6 +157,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
 
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
+    sm.pv_done = 0;
     mbar_init(&sm.q_full, 1);
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&sm.k_full[i], 1);
@@ -282,6 +305,11 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         mma_commit(&sm.o_ready);
         mma_commit(&sm.s_free[j & 1]);
         mma_commit(&sm.kv_empty[slot]);  // V(j) no longer read
+        // wait for PV(j) here (every phase in order) and publish the count, so
+        // the softmax looks at O only when it has to rescale it
+        if (!wait_bar(&sm.o_ready, j & 1, abort_flag)) break;
+        tc_fence_after();
+        asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.pv_done)), "r"(j + 1) : "memory");
       }
     }
   } else {
@@ -364,16 +392,26 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       // nothing visible so far: every p is 0 (and O is rescaled away later)
       const float m_exp = (m_use == NEG_INF) ? 0.f : m_use;
       // p = 2^(s*scale*log2e - m), packed to bf16 pairs and written over S
-      float sk[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial sums
+      // x = s * scale * log2(e) - m and the running sums on packed pairs
+      // (one f32x2 instruction per two scores), p = 2^x on the ex2 unit
+      const uint64_t scale2 = fx::pack2(a.scale_log2, a.scale_log2);
+      const uint64_t negm2 = fx::pack2(-m_exp, -m_exp);
+      uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // 4 independent packed partial sums
       uint32_t pk[KV_TILE / 2];
 #pragma unroll
-      for (int c = 0; c < KV_TILE; c += 2) {
-        const float p0 = ex2(fmaf(s[c], a.scale_log2, -m_exp));
-        const float p1 = ex2(fmaf(s[c + 1], a.scale_log2, -m_exp));
-        sk[(c >> 1) & 3] += p0 + p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
+      for (int e = 0; e < KV_TILE / 2; ++e) {
+        float x0, x1;
+        fx::unpack2(fx::fma2(fx::pack2(s[2 * e], s[2 * e + 1]), scale2, negm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        sum2[e & 3] = fx::add2(sum2[e & 3], fx::pack2(p0, p1));
+        pk[e] = pack_bf16x2(p0, p1);
       }
-      const float rowsum = (sk[0] + sk[1]) + (sk[2] + sk[3]);
+      float rowsum;
+      {
+        float r0, r1;
+        fx::unpack2(fx::add2(fx::add2(sum2[0], sum2[1]), fx::add2(sum2[2], sum2[3])), r0, r1);
+        rowsum = r0 + r1;
+      }
       {
         uint32_t part[32];
 #pragma unroll
@@ -400,17 +438,16 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
-      if (j > 0) {
-        // O holds PV_{j-1} once it completes; needed before a rescale (and it
-        // keeps the o_ready phases consumed in order)
-        if (!__all_sync(0xffffffffu, wait_bar(&sm.o_ready, (j - 1) & 1, abort_flag))) {
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+        // O must hold PV(0..j-1) complete before it is rescaled.  TMEM loads
+        // and stores are warp-collective: the whole warp rescales its rows
+        // together, with factor 1 for rows whose max did not move enough.
+        if (!__all_sync(0xffffffffu, wait_count(&sm.pv_done, j, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // TMEM loads/stores are warp-collective: the whole warp rescales its
-        // rows together, with factor 1 for rows whose max did not move enough
-        if (__any_sync(0xffffffffu, rescale)) {
+        {
           const float f = !rescale ? 1.f : ((m_run == NEG_INF) ? 0.f : ex2(m_run - m_new));
           l_run *= f;
 #pragma unroll
@@ -437,7 +474,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       mbar_arrive(&sm.p_full[j & 1]);
     }
     // epilogue: wait for the last PV, normalise, write
-    if (ok && __all_sync(0xffffffffu, wait_bar(&sm.o_ready, (n_tiles - 1) & 1, abort_flag))) {
+    if (ok && __all_sync(0xffffffffu, wait_count(&sm.pv_done, n_tiles, abort_flag))) {
       tc_fence_after();
       const float inv = 1.f / l_run;
       const float lse2 = m_run + __log2f(l_run);
