@@ -16,8 +16,9 @@
 //              masks, tracks the running max/sum, writes P (bf16) back over S,
 //              rescales O when the max moves by more than 2^8 (exact: the final
 //              normalisation uses the same running max), writes the output.
-//   warp 4     producer: TMEM allocation; TMA loads of the Q tile and of the
-//              K/V tiles (paged blocks: one box per block) into a 3-stage ring.
+//   warp 4     TMEM allocation; TMA loads of the Q tile and of the K tiles
+//   warp 7     TMA loads of the V tiles (paged blocks: one box per block); K
+//              and V each stream through their own 3-stage ring.
 //   warp 5     QK issuer (one thread): S(j) = Q K(j)^T, both operands in
 //              swizzled shared memory, into S buffer j%2 once PV(j-2) (the
 //              last reader of that buffer) has completed (s_free[j%2]).
@@ -44,11 +45,12 @@ namespace {
 
 using namespace sm100;
 
-constexpr int NUM_THREADS = 224;
+constexpr int NUM_THREADS = 256;
 constexpr int SOFTMAX_THREADS = 128;
 constexpr int PRODUCER_WARP = 4;
 constexpr int QK_WARP = 5;
 constexpr int PV_WARP = 6;
+constexpr int V_PRODUCER_WARP = 7;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_O = 0;
 constexpr uint32_t TMEM_S0 = 128;
@@ -73,7 +75,8 @@ struct __align__(1024) Smem {
   uint64_t q_full;
   uint64_t k_full[Cfg<D>::NST];
   uint64_t v_full[Cfg<D>::NST];
-  uint64_t kv_empty[Cfg<D>::NST];
+  uint64_t k_empty[Cfg<D>::NST];  // K slot free: its QK completed
+  uint64_t v_empty[Cfg<D>::NST];  // V slot free: its PV completed
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t s_free[2];  // S buffer b no longer read: PV of its last tile completed
@@ -162,7 +165,8 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.v_full[i], 1);
-      mbar_init(&sm.kv_empty[i], 2);  // released by the QK and the PV issuer
+      mbar_init(&sm.k_empty[i], 1);
+      mbar_init(&sm.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
@@ -178,19 +182,16 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == PRODUCER_WARP) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_kc);
-      tma_prefetch_desc(&tm_vc);
-      tma_prefetch_desc(&tm_kt);
-      tma_prefetch_desc(&tm_vt);
-      mbar_arrive_expect_tx(&sm.q_full, C::Q_BYTES);
-      const int nodes_per_tile = ROW_TILE / a.G;
-      for (int h = 0; h < C::HALVES; ++h)
-        tma_load_4d(sm.q + h * (ROW_TILE * 128), &tm_q, &sm.q_full, 64 * h, g * a.G, rt * nodes_per_tile, b);
-    }
+  // ------------------------------------------------------------ K or V producer
+  // One warp streams the K tiles, another the V tiles: a single warp issues a
+  // TMA request only every ~120 cycles, so one warp alone could not keep up
+  // with 16 paged boxes per tile.  Each ring slot is refilled as soon as its
+  // own consumer (QK for K, PV for V) has released it.
+  auto kv_producer = [&](bool is_v) {
+    const CUtensorMap* tm_pool = is_v ? &tm_vc : &tm_kc;
+    const CUtensorMap* tm_node = is_v ? &tm_vt : &tm_kt;
+    uint64_t* full = is_v ? sm.v_full : sm.k_full;
+    uint64_t* empty = is_v ? sm.v_empty : sm.k_empty;
     const int boxes = KV_TILE / args.box_rows;  // boxes (paged blocks) per tile (1 .. 8)
     const uint32_t box_bytes = args.box_rows * D * 2;
     // Block-table entries are software-pipelined: lane L holds the entry of
@@ -214,7 +215,8 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     int grp_nxt = (n_prefix > tpg) ? load_group(1) : 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int slot = j % C::NST;
-      if (j >= C::NST && !__all_sync(0xffffffffu, wait_bar(&sm.kv_empty[slot], ((j / C::NST) - 1) & 1, abort_flag)))
+      uint8_t* dst = is_v ? sm.v[slot] : sm.k[slot];
+      if (j >= C::NST && !__all_sync(0xffffffffu, wait_bar(&empty[slot], ((j / C::NST) - 1) & 1, abort_flag)))
         break;
       if (j < n_prefix) {
         if (j > 0 && j % tpg == 0) {
@@ -229,29 +231,35 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         const bool issue = lane < boxes && t0 < P;
         const int row0 = t0 % a.bs;
         const unsigned mask = __ballot_sync(0xffffffffu, issue);
-        const uint32_t bytes = __popc(mask) * box_bytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.k_full[slot], bytes);
-          mbar_arrive_expect_tx(&sm.v_full[slot], bytes);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], __popc(mask) * box_bytes);
         __syncwarp();
-        if (issue) {
-          // one box = every D column of box_rows tokens of one paged block
-          const int z = blk * a.Hkv + g;
-          tma_load_5d(sm.k[slot] + lane * box_bytes, &tm_kc, &sm.k_full[slot], 0, 0, 0, row0 >> 3, z);
-          tma_load_5d(sm.v[slot] + lane * box_bytes, &tm_vc, &sm.v_full[slot], 0, 0, 0, row0 >> 3, z);
-        }
+        // one box = every D column of box_rows tokens of one paged block
+        if (issue) tma_load_5d(dst + lane * box_bytes, tm_pool, &full[slot], 0, 0, 0, row0 >> 3, blk * a.Hkv + g);
       } else if (lane == 0) {
         const int n0 = (j - n_prefix) * KV_TILE;  // first tree node of this tile; nodes >= N read as zeros
-        mbar_arrive_expect_tx(&sm.k_full[slot], C::TILE_BYTES);
-        mbar_arrive_expect_tx(&sm.v_full[slot], C::TILE_BYTES);
-        for (int h = 0; h < C::HALVES; ++h)
-          tma_load_4d(sm.k[slot] + h * C::HALF_BYTES, &tm_kt, &sm.k_full[slot], 64 * h, g, n0, b);
-        for (int h = 0; h < C::HALVES; ++h)
-          tma_load_4d(sm.v[slot] + h * C::HALF_BYTES, &tm_vt, &sm.v_full[slot], 64 * h, g, n0, b);
+        mbar_arrive_expect_tx(&full[slot], C::TILE_BYTES);
+        for (int h = 0; h < C::HALVES; ++h) tma_load_4d(dst + h * C::HALF_BYTES, tm_node, &full[slot], 64 * h, g, n0, b);
       }
       __syncwarp();
     }
+  };
+
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------ Q and K producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_kc);
+      tma_prefetch_desc(&tm_vc);
+      tma_prefetch_desc(&tm_kt);
+      tma_prefetch_desc(&tm_vt);
+      mbar_arrive_expect_tx(&sm.q_full, C::Q_BYTES);
+      const int nodes_per_tile = ROW_TILE / a.G;
+      for (int h = 0; h < C::HALVES; ++h)
+        tma_load_4d(sm.q + h * (ROW_TILE * 128), &tm_q, &sm.q_full, 64 * h, g * a.G, rt * nodes_per_tile, b);
+    }
+    kv_producer(false);
+  } else if (warp == V_PRODUCER_WARP) {
+    kv_producer(true);
   } else if (warp == QK_WARP) {
     // ------------------------------------------------------------ QK issuer
     if (lane == 0) {
@@ -281,7 +289,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
                  k > 0);
         }
         mma_commit(&sm.s_full[j & 1]);
-        mma_commit(&sm.kv_empty[slot]);  // K(j) no longer read
+        mma_commit(&sm.k_empty[slot]);  // K(j) no longer read
       }
     }
   } else if (warp == PV_WARP) {
@@ -304,7 +312,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
                  j > 0 || k > 0);
         mma_commit(&sm.o_ready);
         mma_commit(&sm.s_free[j & 1]);
-        mma_commit(&sm.kv_empty[slot]);  // V(j) no longer read
+        mma_commit(&sm.v_empty[slot]);  // V(j) no longer read
         // wait for PV(j) here (every phase in order) and publish the count, so
         // the softmax looks at O only when it has to rescale it
         if (!wait_bar(&sm.o_ready, j & 1, abort_flag)) break;
