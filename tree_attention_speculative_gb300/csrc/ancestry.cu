@@ -20,6 +20,8 @@ k_ancestry(const int32_t* __restrict__ parent, const int32_t* __restrict__ prefi
   __shared__ int sp[MAX_NODES];
   const int b = blockIdx.x;
   const int i = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   int p = -1;
   bool ok = true;
   if (i < N) {
@@ -61,8 +63,8 @@ cudaError_t launch_ancestry(const int32_t* parent, const int32_t* prefix_len, in
                             uint64_t* anc, int32_t* depth, int32_t* pos, int32_t* status,
                             cudaStream_t s) {
   const int threads = ceil_div(N, 32) * 32;
-  k_ancestry<<<B, threads, 0, s>>>(parent, prefix_len, N, ceil_div(N, 64), anc, depth, pos, status);
-  return cudaGetLastError();
+  return launch_pdl(k_ancestry, dim3(B), dim3(threads), 0, s, parent, prefix_len, N, ceil_div(N, 64), anc, depth,
+                    pos, status);
 }
 
 }  // namespace ts

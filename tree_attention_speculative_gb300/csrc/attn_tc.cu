@@ -147,17 +147,6 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   const int rt = blockIdx.x, split = blockIdx.y, unit = blockIdx.z;
   const int b = unit / a.Hkv, g = unit - b * a.Hkv;
 
-  int P;
-  const bool p_ok = usable_prefix(a.prefix_len[b], a.chunk_tiles, a.max_splits, a.bs, a.max_blocks, &P);
-  const int tiles = prefix_tiles(P);
-  const int ns = num_splits(P, a.chunk_tiles);
-  if (split >= ns) return;  // whole CTA leaves before any barrier or TMEM use
-  if (!p_ok && threadIdx.x == 0 && rt == 0 && split == 0 && a.status) a.status[b] = TS_ERR_SHAPE;
-  const int t_begin = split * a.chunk_tiles;
-  const int n_prefix = min(tiles, t_begin + a.chunk_tiles) - t_begin;
-  const int n_tree = (split == ns - 1) ? ceil_div(a.N, KV_TILE) : 0;
-  const int n_tiles = n_prefix + n_tree;
-
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
     sm.pv_done = 0;
@@ -181,6 +170,23 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+
+  // everything above touched no global memory and overlaps the previous
+  // kernel's tail; wait for it before reading any input.  The next kernel is
+  // released only at this CTA's teardown: this kernel can run many waves, and
+  // the next kernel's CTAs should not wait on SMs the later waves need.
+  pdl_wait();
+  int P;
+  const bool p_ok = usable_prefix(a.prefix_len[b], a.chunk_tiles, a.max_splits, a.bs, a.max_blocks, &P);
+  const int tiles = prefix_tiles(P);
+  const int ns = num_splits(P, a.chunk_tiles);
+  const bool has_work = split < ns;  // splits past this sequence's prefix have nothing to do
+  if (!p_ok && threadIdx.x == 0 && rt == 0 && split == 0 && a.status) a.status[b] = TS_ERR_SHAPE;
+  const int t_begin = split * a.chunk_tiles;
+  const int n_prefix = min(tiles, t_begin + a.chunk_tiles) - t_begin;
+  const int n_tree = (split == ns - 1) ? ceil_div(a.N, KV_TILE) : 0;
+  const int n_tiles = n_prefix + n_tree;
+
 
   // ------------------------------------------------------------ K or V producer
   // One warp streams the K tiles, another the V tiles: a single warp issues a
@@ -244,7 +250,9 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     }
   };
 
-  if (warp == PRODUCER_WARP) {
+  if (!has_work) {
+    // nothing to do; fall through to the teardown
+  } else if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -526,6 +534,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
 
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();
   if (sm.abort_flag && threadIdx.x == 0 && a.status) a.status[b] = TS_ERR_TIMEOUT;
   if (warp == PRODUCER_WARP) {
     tc_fence_after();
@@ -571,8 +580,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
     if (!encode_bf16_sw128(&m_vt, a.v_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
   dim3 grid(a.row_tiles, a.max_splits, a.B * a.Hkv);
-  k_attn_tc<D><<<grid, NUM_THREADS, smem_bytes<D>(), s>>>(t, m_q, m_kc, m_vc, m_kt, m_vt);
-  return cudaGetLastError();
+  return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt);
 }
 
 }  // namespace

@@ -19,6 +19,8 @@ k_combine(AttnArgs a) {
   const int rows = a.B * a.N * a.Hq;
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   if (row >= rows) return;
   const int b = row / (a.N * a.Hq);
   int P;
@@ -77,11 +79,8 @@ k_combine(AttnArgs a) {
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s) {
   const int rows = a.B * a.N * a.Hq;
   const int grid = ceil_div(rows, 8);
-  if (a.D == 128)
-    k_combine<128><<<grid, 256, 0, s>>>(a);
-  else
-    k_combine<64><<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return a.D == 128 ? launch_pdl(k_combine<128>, dim3(grid), dim3(256), 0, s, a)
+                   : launch_pdl(k_combine<64>, dim3(grid), dim3(256), 0, s, a);
 }
 
 }  // namespace ts

@@ -5,9 +5,35 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "treespec.h"
 
 namespace ts {
+
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may start while the previous kernel in the stream finishes; each one
+// runs only its set-up (no global memory) before pdl_wait(), which returns once
+// the previous kernel has completed and its writes are visible, and then calls
+// pdl_trigger() to let the next kernel begin its own set-up.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Prefix keys are processed in tiles of KV_TILE tokens; packed query rows in
 // tiles of ROW_TILE rows (one MMA M extent).

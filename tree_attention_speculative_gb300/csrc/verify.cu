@@ -62,6 +62,8 @@ __device__ __forceinline__ void block_argmax(float& v, int& i) {
 
 __global__ void __launch_bounds__(VERIFY_THREADS)
 k_verify(VerifyArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x / a.chunks;
   const int chunk = blockIdx.x - row * a.chunks;
   const int b = row / a.N;
@@ -207,8 +209,7 @@ k_verify(VerifyArgs a) {
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   const int grid = a.B * a.N * a.chunks;
-  k_verify<<<grid, VERIFY_THREADS, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_verify, dim3(grid), dim3(VERIFY_THREADS), 0, s, a);
 }
 
 // ---------------------------------------------------------------------------
