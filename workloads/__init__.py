@@ -243,14 +243,15 @@ def planted_logits(g: np.random.Generator, parent: np.ndarray, draft: np.ndarray
 # paged KV pool
 # ----------------------------------------------------------------------------
 
-def paged_layout(g: np.random.Generator, prefix_len: np.ndarray, bs: int, permute: bool):
+def paged_layout(g: np.random.Generator, prefix_len: np.ndarray, bs: int, permute: bool, spare: int = 0):
     """Block table for per-sequence prefixes over a shared pool of ``bs``-token blocks.
 
-    The pool holds exactly sum_b ceil(P_b / bs) blocks (at least one in total);
-    with ``permute`` the block ids are a random permutation, otherwise sequence b
-    owns a contiguous run.  Unused table entries are -1.
+    The pool holds exactly sum_b ceil((P_b + spare) / bs) blocks (at least one in
+    total): ``spare`` tokens of room per sequence past its prefix (for appending
+    accepted tokens).  With ``permute`` the block ids are a random permutation,
+    otherwise sequence b owns a contiguous run.  Unused table entries are -1.
     """
-    nblk = [-(-int(p) // bs) for p in prefix_len]
+    nblk = [-(-(int(p) + spare) // bs) for p in prefix_len]
     total = max(1, sum(nblk))
     ids = g.permutation(total).astype(np.int32) if permute else np.arange(total, dtype=np.int32)
     maxb = max(1, max(nblk))
@@ -308,7 +309,7 @@ class Case:
 def build_case(name: str, seed: int, parent: np.ndarray, prefix_len, Hq: int, Hkv: int, D: int,
                bs: int, permute: bool, vocab: int = 0, plant_len=None, hot_key_frac: float = 0.0,
                hot_key_scale: float = 8.0, scale: Optional[float] = None,
-               plant_target=None) -> Case:
+               plant_target=None, spare_tokens: int = 0) -> Case:
     """Draw every tensor of one verification step.
 
     ``parent`` is [N] (shared by the batch) or [B, N].  ``prefix_len`` is [B].
@@ -325,7 +326,7 @@ def build_case(name: str, seed: int, parent: np.ndarray, prefix_len, Hq: int, Hk
         parent = np.tile(parent, (B, 1))
     N = parent.shape[1]
     g = rng(seed, "structure")
-    table, nblocks = paged_layout(g, prefix_len, bs, permute)
+    table, nblocks = paged_layout(g, prefix_len, bs, permute, spare_tokens)
 
     row_k_cache = row_k_tree = None
     if hot_key_frac > 0.0:
