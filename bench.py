@@ -509,6 +509,85 @@ WORKLOAD_DESC = {
 }
 
 
+def run_commit(args, world, rank, local):
+    """--part commit: time tree_commit_accepted (appending every sequence's accepted
+    path to its paged cache) on the workload, after one real verification step."""
+    import torch
+    import workloads as W
+    import oracle
+    from tree_attention_speculative_gb300 import _build
+    _build.build()
+    import tree_attention_speculative_gb300 as ts
+    from tree_attention_speculative_gb300.step import TreeVerifyStep
+    from tests.gpu_util import to_dev
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kw = workload_overrides(args)
+    probe = W.make(args.workload, **kw)
+    if not probe.vocab:
+        raise SystemExit("--part commit needs a workload with logits (c1, c2, c4, c5)")
+    depth = int(max(oracle.tree.depths(p).max() for p in probe.parent))
+    del probe
+    case = W.make(args.workload, spare_tokens=depth + 1, **kw)
+    t = to_dev(case, dev)
+    st = TreeVerifyStep(case.B, case.N, case.Hq, case.Hkv, case.D, case.prefix_len, vocab=case.vocab,
+                        max_depth=depth, device=dev)
+    st.run(t["parent"], t["prefix_len"], t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["k_tree"],
+           t["v_tree"], t["draft"], t["logits"])
+    torch.cuda.synchronize()
+    new_len = torch.empty_like(t["prefix_len"])
+
+    def commit():
+        ts.tree_commit_accepted(t["k_tree"], t["v_tree"], st.accepted, st.accept_len, t["prefix_len"],
+                                t["k_cache"], t["v_cache"], t["block_table"], new_len, st.status)
+
+    for _ in range(args.warmup):
+        commit()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(args.steps):
+            commit()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    L = st.accept_len.cpu().numpy()
+    assert (st.status.cpu().numpy() == 0).all()
+    tokens = int((L + 1).sum())
+    nbytes = tokens * case.Hkv * case.D * 2 * 2 * 2 + case.B * 4 * 4   # read tree + write cache, K and V
+    pk = peaks()
+    acc = st.accepted.cpu().numpy()
+    c0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - c0 < 2.0 or reps < 1:
+        oracle.commit.commit_accepted(case.k_tree, case.v_tree, acc, L, np.zeros(case.B, np.int32), case.prefix_len,
+                                      case.k_cache, case.v_cache, case.block_table)
+        reps += 1
+    t_cpu = (time.perf_counter() - c0) / reps
+    line = {
+        "metric": "commit of accepted paths: tokens appended/s", "value": tokens / (ms * 1e-3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: " + WORKLOAD_DESC[args.workload], "part": "commit",
+                   "tokens_per_step": tokens, "timing": "CUDA graph of the commit call alone, CUDA events"},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "traffic": None,
+                     "kernel": "tree_commit_accepted", "algorithmic_bytes": nbytes},
+        "gpu_launches": args.steps,
+        "cpu_baseline": {"value": tokens / t_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"the whole commit of this workload, {reps} repeats"},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: rank 0 alone, on the host cores."""
     if rank != 0:
@@ -561,6 +640,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch of c4 (smaller profiling case)")
     ap.add_argument("--prefix", type=int, default=0, help="override the prefix length of c5")
+    ap.add_argument("--part", choices=["step", "commit"], default="step",
+                    help="step: the verification step (default); commit: append accepted paths to the cache")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -569,6 +650,8 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.part == "commit":
+        run_commit(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

@@ -216,6 +216,40 @@ TS_API ts_status tree_verify_greedy(const int32_t* draft_tokens, const float* ta
                              int32_t* argmax_out, int32_t* status, void* workspace,
                              size_t workspace_bytes, ts_stream stream);
 
+/*
+ * tree_commit_accepted — append the accepted path's keys/values to the cache.
+ *
+ * [P1] Key Mechanisms > Speculative KV Cache Reuse (the tree's keys/values are
+ * reused), Multi-Token Acceptance & Rollback (keep the accepted path, discard
+ * the rejected branches) and Integration with Speculative Decoding (append the
+ * accepted prefix and continue from the new state).  The root (the last
+ * verified token, attended at position P_b) and the accepted drafts x1..n*
+ * become prefix tokens P_b .. P_b + L; rejected branches need no work, their
+ * keys/values never entered the cache.
+ *
+ *   k_tree, v_tree   [B, N, Hkv, D] bf16, the tree's keys/values (as given to
+ *                    tree_attn_fwd).
+ *   accepted         [B, max_depth + 1] int32 and accept_len [B] int32 from
+ *                    tree_verify_greedy.
+ *   prefix_len       [B] int32, P_b before the commit.
+ *   k_cache, v_cache [num_blocks, Hkv, block_size, D] bf16, written at rows
+ *                    (t mod block_size) of blocks block_table[b, t div
+ *                    block_size] for t = P_b .. P_b + L; nothing else changes.
+ *                    The caller provides blocks for every position committed.
+ *   new_prefix_len   [B] int32 out: P_b + L + 1 (may be the prefix_len array).
+ *   status           [B] int32 in/out (or NULL): a sequence whose status is
+ *                    not 0 commits nothing and keeps P_b; a destination block
+ *                    or node id out of range commits nothing for that
+ *                    sequence and sets TS_ERR_BAD_BLOCK.
+ * Returns TS_ERR_NULL / TS_ERR_SHAPE / TS_ERR_UNSUPPORTED (D not 64 or 128) /
+ * TS_ERR_CUDA.
+ */
+TS_API ts_status tree_commit_accepted(const void* k_tree, const void* v_tree, const int32_t* accepted,
+                                      const int32_t* accept_len, const int32_t* prefix_len, void* k_cache,
+                                      void* v_cache, const int32_t* block_table, int B, int N, int Hkv, int D,
+                                      int block_size, int num_blocks, int max_blocks, int max_depth,
+                                      int32_t* new_prefix_len, int32_t* status, ts_stream stream);
+
 /* Size of the library-owned scratch behind tree_verify_greedy_noalloc. */
 #define TS_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 

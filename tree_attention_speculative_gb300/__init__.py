@@ -21,7 +21,7 @@ from ._build import LIB as LIB_PATH
 __all__ = [
     "TreeSpecError", "lib", "ts_status_str", "tree_build_ancestry", "AttnParams", "attn_params",
     "tree_attn_workspace_size", "tree_attn_fwd", "tree_verify_workspace_size", "tree_verify_greedy",
-    "tree_verify_greedy_noalloc", "NOALLOC_SCRATCH_BYTES", "STATUS",
+    "tree_verify_greedy_noalloc", "tree_commit_accepted", "NOALLOC_SCRATCH_BYTES", "STATUS",
 ]
 
 STATUS = {
@@ -53,7 +53,8 @@ _LIB: Optional[ctypes.CDLL] = None
 
 # every symbol include/treespec.h declares
 EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_fwd",
-           "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc")
+           "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc",
+           "tree_commit_accepted")
 
 # TS_VERIFY_NOALLOC_SCRATCH_BYTES of treespec.h
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -81,6 +82,9 @@ def lib() -> ctypes.CDLL:
         L.tree_verify_greedy.restype = i32
         L.tree_verify_greedy_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.tree_verify_greedy_noalloc.restype = i32
+        L.tree_commit_accepted.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                           vp, vp, vp]
+        L.tree_commit_accepted.restype = i32
         _LIB = L
     return _LIB
 
@@ -155,6 +159,17 @@ def tree_verify_greedy(draft_tokens, target_logits, parent_idx, max_depth: int, 
                                     _p(accepted), _p(accept_len), _p(bonus), _p(argmax_out), _p(status),
                                     _p(workspace), workspace.numel() * workspace.element_size(), _s(stream)),
            "tree_verify_greedy")
+
+
+def tree_commit_accepted(k_tree, v_tree, accepted, accept_len, prefix_len, k_cache, v_cache, block_table,
+                         new_prefix_len, status=None, stream=None) -> None:
+    """Append the accepted path (root .. n*) of every sequence to the paged cache."""
+    B, N, Hkv, D = k_tree.shape
+    nblk, _, bs, _ = k_cache.shape
+    _check(lib().tree_commit_accepted(_p(k_tree), _p(v_tree), _p(accepted), _p(accept_len), _p(prefix_len),
+                                      _p(k_cache), _p(v_cache), _p(block_table), B, N, Hkv, D, bs, nblk,
+                                      block_table.shape[1], accepted.shape[1] - 1, _p(new_prefix_len), _p(status),
+                                      _s(stream)), "tree_commit_accepted")
 
 
 def tree_verify_greedy_noalloc(draft_tokens, target_logits, parent_idx, max_depth: int, accepted, accept_len, bonus,

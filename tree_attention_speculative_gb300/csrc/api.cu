@@ -241,6 +241,35 @@ ts_status tree_verify_greedy(const int32_t* draft_tokens, const float* target_lo
   return launch_verify(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
+ts_status tree_commit_accepted(const void* k_tree, const void* v_tree, const int32_t* accepted,
+                               const int32_t* accept_len, const int32_t* prefix_len, void* k_cache, void* v_cache,
+                               const int32_t* block_table, int B, int N, int Hkv, int D, int block_size,
+                               int num_blocks, int max_blocks, int max_depth, int32_t* new_prefix_len,
+                               int32_t* status, ts_stream stream) {
+  if (!k_tree || !v_tree || !accepted || !accept_len || !prefix_len || !k_cache || !v_cache || !block_table ||
+      !new_prefix_len)
+    return TS_ERR_NULL;
+  if (B < 1 || N < 1 || N > MAX_NODES || Hkv < 1 || block_size < 1 || num_blocks < 1 || max_blocks < 1 ||
+      max_depth < 0)
+    return TS_ERR_SHAPE;
+  if (D != 64 && D != 128) return TS_ERR_UNSUPPORTED;
+  if (!aligned16(k_tree) || !aligned16(v_tree) || !aligned16(k_cache) || !aligned16(v_cache)) return TS_ERR_SHAPE;
+  CommitArgs a{};
+  a.k_tree = static_cast<const __nv_bfloat16*>(k_tree);
+  a.v_tree = static_cast<const __nv_bfloat16*>(v_tree);
+  a.accepted = accepted;
+  a.accept_len = accept_len;
+  a.prefix_len = prefix_len;
+  a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  a.block_table = block_table;
+  a.new_prefix_len = new_prefix_len;
+  a.status = status;
+  a.B = B; a.N = N; a.Hkv = Hkv; a.D = D; a.bs = block_size; a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks; a.max_depth = max_depth;
+  return launch_commit(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
 ts_status tree_verify_greedy_noalloc(const int32_t* draft_tokens, const float* target_logits,
                                      const int32_t* parent_idx, int B, int N, int V, int max_depth,
                                      int32_t* accepted, int32_t* accept_len, int32_t* bonus,

@@ -130,4 +130,19 @@ constexpr int VERIFY_CHUNK = 8192;  // logits per CTA
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
 ts_status verify_static_scratch(void** ptr, size_t* bytes);
 
+struct CommitArgs {
+  const __nv_bfloat16* k_tree;
+  const __nv_bfloat16* v_tree;
+  const int32_t* accepted;
+  const int32_t* accept_len;
+  const int32_t* prefix_len;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  const int32_t* block_table;
+  int32_t* new_prefix_len;
+  int32_t* status;
+  int B, N, Hkv, D, bs, num_blocks, max_blocks, max_depth;
+};
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
+
 }  // namespace ts

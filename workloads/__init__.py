@@ -370,14 +370,14 @@ def build_case(name: str, seed: int, parent: np.ndarray, prefix_len, Hq: int, Hk
 
 # The five workloads.  Seeds: 20260000 + k unless overridden.
 
-def c1(seed: int = 20260001) -> Case:
+def c1(seed: int = 20260001, **extra) -> Case:
     """Tiny reference: batch 1, the five-node demo tree, prefix 16, 2 heads (no GQA),
     head_dim 64; vocab 1000 with the greedy path 0 -> 1 -> 3 planted."""
     return build_case("c1", seed, tree_worked_example(), [16], Hq=2, Hkv=2, D=64, bs=16,
-                      permute=False, vocab=1000, plant_len=2, plant_target=[3])
+                      permute=False, vocab=1000, plant_len=2, plant_target=[3], **extra)
 
 
-def c2(seed: int = 20260002, vocab: int = 128256) -> Case:
+def c2(seed: int = 20260002, vocab: int = 128256, **extra) -> Case:
     """Llama-3-8B-shaped layer: batch 1, 32 q / 8 kv heads, head_dim 128, contiguous
     4096-token prefix, a random 64-node tree of depth 6.  The workload lists no
     logits for this shape; the verification step here draws them over the
@@ -386,21 +386,21 @@ def c2(seed: int = 20260002, vocab: int = 128256) -> Case:
     parent = tree_random_levels(g, 64, 6)
     plant = int(rng(seed, "plant").integers(0, 7))
     case = build_case("c2", seed, parent, [4096], Hq=32, Hkv=8, D=128, bs=4096, permute=False,
-                      vocab=vocab, plant_len=plant)
+                      vocab=vocab, plant_len=plant, **extra)
     return case
 
 
-def c3(seed: int = 20260003) -> Case:
+def c3(seed: int = 20260003, **extra) -> Case:
     """Batched serving: batch 16, prefixes uniform in [1024, 16384], 32 q / 8 kv heads,
     head_dim 128, paged KV (block 16, permuted table), the fixed 26-node tree with
     widths [4, 3, 2, 1, 1] shared by the batch.  Attention only."""
     g = rng(seed, "prefix")
     plen = g.integers(1024, 16385, size=16).astype(np.int32)
     parent = tree_from_widths([4, 3, 2, 1, 1])
-    return build_case("c3", seed, parent, plen, Hq=32, Hkv=8, D=128, bs=16, permute=True)
+    return build_case("c3", seed, parent, plen, Hq=32, Hkv=8, D=128, bs=16, permute=True, **extra)
 
 
-def c4(seed: int = 20260004, batch: int = 64) -> Case:
+def c4(seed: int = 20260004, batch: int = 64, **extra) -> Case:
     """70B-shaped layer: batch 64, 64 q / 8 kv heads, head_dim 128, paged KV (block 16),
     prefix 8192; per-sequence random 64-node trees of depth 8; logits over 128256
     with planted accepted lengths uniform in [0, 8]."""
@@ -408,10 +408,10 @@ def c4(seed: int = 20260004, batch: int = 64) -> Case:
     parents = np.stack([tree_random_levels(g, 64, 8) for _ in range(batch)])
     plant = rng(seed, "plant").integers(0, 9, size=batch)
     return build_case("c4", seed, parents, [8192] * batch, Hq=64, Hkv=8, D=128, bs=16,
-                      permute=True, vocab=128256, plant_len=plant)
+                      permute=True, vocab=128256, plant_len=plant, **extra)
 
 
-def c5(seed: int = 20260005, prefix: int = 131072) -> Case:
+def c5(seed: int = 20260005, prefix: int = 131072, **extra) -> Case:
     """Long-context wide tree: batch 4, prefix 131072, 32 q / 8 kv heads, head_dim 128,
     paged KV (block 64); a random 192-node tree of depth 10; 1% of key rows scaled by
     8; logits over 128256.  No accepted length is given for this shape; one uniform
@@ -420,11 +420,12 @@ def c5(seed: int = 20260005, prefix: int = 131072) -> Case:
     parents = np.stack([tree_random_levels(g, 192, 10) for _ in range(4)])
     plant = rng(seed, "plant").integers(0, 11, size=4)
     return build_case("c5", seed, parents, [prefix] * 4, Hq=32, Hkv=8, D=128, bs=64,
-                      permute=True, vocab=128256, plant_len=plant, hot_key_frac=0.01)
+                      permute=True, vocab=128256, plant_len=plant, hot_key_frac=0.01, **extra)
 
 
 CONFIGS = {"c1": c1, "c2": c2, "c3": c3, "c4": c4, "c5": c5}
 
 
 def make(name: str, **kw) -> Case:
+    """A named workload; extra keywords (e.g. ``spare_tokens``) go to ``build_case``."""
     return CONFIGS[name](**kw)
