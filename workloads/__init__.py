@@ -368,6 +368,60 @@ def build_case(name: str, seed: int, parent: np.ndarray, prefix_len, Hq: int, Hk
     return case
 
 
+# ----------------------------------------------------------------------------
+# inputs of stochastic (temperature) verification
+# ----------------------------------------------------------------------------
+
+@dataclass
+class StochasticInputs:
+    """What a sampled verification step consumes besides the tree."""
+    draft: np.ndarray        # [B, N] int32; children of u drawn without replacement from q[u]
+    logits: np.ndarray       # [B, N, V] fp32 target logits
+    q: np.ndarray            # [B, N, V] fp32 draft probabilities (each row sums to 1 in fp64)
+    coins: np.ndarray        # [B, N] fp32 uniforms in [0, 1)
+    temperature: float
+
+
+def stochastic_inputs(seed: int, parent: np.ndarray, vocab: int, temperature: float = 1.0,
+                      logit_scale: float = 2.0, draft_noise: float = 0.5,
+                      tag: str = "stoch") -> StochasticInputs:
+    """Target logits, a draft model's distributions, sampled draft tokens and coins.
+
+    Target logits are ``logit_scale`` * N(0, 1).  The draft model is modelled as
+    the target with its logits perturbed by ``draft_noise`` * N(0, 1): its
+    distribution at node u is that perturbed row at temperature T, normalised
+    in fp64 and stored in fp32.  The children of every node take tokens drawn
+    from the parent's draft distribution without replacement, in index order
+    (the ordered top-k of log q + Gumbel noise).  The coins are the uniforms
+    the verifier consumes.
+    """
+    parent = np.asarray(parent, np.int32)
+    B, N = parent.shape
+    logits = normal_f32(seed, f"{tag}-target", (B, N, vocab)) * np.float32(logit_scale)
+    noise = normal_f32(seed, f"{tag}-draft", (B, N, vocab))
+    q = np.empty((B, N, vocab), np.float32)
+    draft = np.zeros((B, N), np.int32)
+
+    def one(b):
+        z = (logits[b].astype(np.float64) + draft_noise * noise[b].astype(np.float64)) / temperature
+        w = np.exp(z - z.max(axis=1, keepdims=True))
+        q[b] = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+        g = rng(seed, f"{tag}-tokens{b}")
+        for u, kids in enumerate(_children_of(parent[b])):
+            if not kids:
+                continue
+            qu = q[b, u].astype(np.float64)
+            with np.errstate(divide="ignore"):
+                key = np.log(qu) - np.log(-np.log(g.random(vocab)))
+            top = np.argpartition(-key, len(kids) - 1)[: len(kids)]
+            top = top[np.argsort(-key[top], kind="stable")]
+            draft[b, kids] = top.astype(np.int32)
+
+    list(_pool().map(one, range(B)))
+    coins = rng(seed, f"{tag}-coins").random((B, N), dtype=np.float32)
+    return StochasticInputs(draft=draft, logits=logits, q=q, coins=coins, temperature=float(temperature))
+
+
 # The five workloads.  Seeds: 20260000 + k unless overridden.
 
 def c1(seed: int = 20260001, **extra) -> Case:
