@@ -588,6 +588,110 @@ def run_commit(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_stochastic(args, world, rank, local):
+    """--part stochastic: time tree_verify_stochastic (rejection-sampling
+    verification at --temperature) on the workload's trees."""
+    import torch
+    import workloads as W
+    import oracle
+    from tree_attention_speculative_gb300 import _build
+    _build.build()
+    import tree_attention_speculative_gb300 as ts
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    batch = args.batch or 64
+    if args.batch and args.workload != "c4":
+        raise SystemExit("--batch applies to c4 only")
+    # two input sets, used alternately: a call never finds the previous call's rows in L2
+    sets = []
+    for k in range(2):
+        parent, si = W.stochastic_workload(args.workload, temperature=args.temperature, batch=batch, tag=f"stoch{k}")
+        sets.append((parent, si))
+    parent = sets[0][0]
+    B, N = parent.shape
+    V = sets[0][1].logits.shape[2]
+    depth = int(max(oracle.tree.depths(p).max() for p in parent))
+    dsets = []
+    for _, si in sets:
+        dsets.append(dict(draft=torch.from_numpy(si.draft).to(dev), logits=torch.from_numpy(si.logits).to(dev),
+                          q=torch.from_numpy(si.q).to(dev), coins=torch.from_numpy(si.coins).to(dev)))
+    par = torch.from_numpy(np.ascontiguousarray(parent, np.int32)).to(dev)
+    outs = [dict(acc=torch.empty((B, depth + 1), dtype=torch.int32, device=dev),
+                 L=torch.empty(B, dtype=torch.int32, device=dev), bonus=torch.empty(B, dtype=torch.int32, device=dev),
+                 st=torch.zeros(B, dtype=torch.int32, device=dev)) for _ in range(2)]
+
+    def call(k):
+        d, o = dsets[k], outs[k]
+        ts.tree_verify_stochastic(d["draft"], d["logits"], d["q"], par, d["coins"], args.temperature, o["acc"],
+                                  o["L"], o["bonus"], o["st"])
+
+    for i in range(args.warmup):
+        call(i & 1)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(args.steps):
+            call(i & 1)
+    g.replay()
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    # rows the walks had to read: every visited node's logits, plus its draft row when it has children
+    nbytes = 0
+    for k in range(2):
+        L = outs[k]["L"].cpu().numpy()
+        acc = outs[k]["acc"].cpu().numpy()
+        assert (outs[k]["st"].cpu().numpy() == 0).all()
+        for b in range(B):
+            kids = np.bincount(parent[b][1:], minlength=N)
+            for u in acc[b][: L[b] + 1]:
+                nbytes += V * 4 * (2 if kids[u] else 1)
+    nbytes = nbytes / 2 + B * N * 4 * 3   # per call; + drafts, parents, coins
+    pk = peaks()
+    parent0, si0 = sets[0]
+    c0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - c0 < 3.0 or reps < 1:
+        oracle.stochastic.verify_stochastic(si0.draft, si0.logits, si0.q, parent0, si0.coins, args.temperature, depth)
+        reps += 1
+    t_cpu = (time.perf_counter() - c0) / reps
+    lens = np.concatenate([o["L"].cpu().numpy() for o in outs])
+    line = {
+        "metric": "stochastic tree verification: tree tokens verified/s", "value": B * N / (ms * 1e-3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload} trees, vocab {V}, B{B}, N{N}; logits 2*N(0,1), draft = target "
+                               f"logits + 0.5*N(0,1), temperature {args.temperature}",
+                   "part": "stochastic", "mean_accept_len": float(lens.mean()),
+                   "timing": "CUDA graph of the call alone, CUDA events; two input sets alternate, so no call "
+                             "finds its rows in L2"},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "traffic": None,
+                     "kernel": "tree_verify_stochastic", "algorithmic_bytes": nbytes,
+                     "note": "bytes = rows of the visited nodes only (the walk is sequential per sequence)"},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "cpu_baseline": {"value": B * N / t_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"the whole batch of this workload, {reps} repeats"},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: rank 0 alone, on the host cores."""
     if rank != 0:
@@ -640,8 +744,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch of c4 (smaller profiling case)")
     ap.add_argument("--prefix", type=int, default=0, help="override the prefix length of c5")
-    ap.add_argument("--part", choices=["step", "commit"], default="step",
-                    help="step: the verification step (default); commit: append accepted paths to the cache")
+    ap.add_argument("--part", choices=["step", "commit", "stochastic"], default="step",
+                    help="step: the verification step (default); commit: append accepted paths to the cache; "
+                         "stochastic: rejection-sampling verification")
+    ap.add_argument("--temperature", type=float, default=1.0, help="sampling temperature of --part stochastic")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -652,6 +758,8 @@ def main(argv=None):
         run_reference(args, world, rank)
     elif args.part == "commit":
         run_commit(args, world, rank, local)
+    elif args.part == "stochastic":
+        run_stochastic(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

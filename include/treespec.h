@@ -250,6 +250,55 @@ TS_API ts_status tree_commit_accepted(const void* k_tree, const void* v_tree, co
                                       int block_size, int num_blocks, int max_blocks, int max_depth,
                                       int32_t* new_prefix_len, int32_t* status, ts_stream stream);
 
+/*
+ * tree_verify_stochastic — temperature verification by rejection sampling.
+ *
+ * [P3] Production Inference Runtimes section: each accepted token is checked
+ * against the target model's own distribution by rejection sampling, so the
+ * emitted tokens follow the target exactly; [P3] code listing (comment of
+ * verify_candidate_tree): greedy or temperature-sampled target predictions;
+ * [P1] Key Mechanisms > Multi-Token Acceptance & Rollback.  The pages give no
+ * rule for several drafts under one node; this call takes the siblings, drawn
+ * from the draft distribution without replacement, in index order:
+ *   r = softmax(target_logits[u] / temperature), q' = draft_probs[u];
+ *   child c (token x) is accepted iff coins[c] * q'(x) < r(x), and the walk
+ *   moves to c;  otherwise r <- max(r - q', 0) renormalised (unchanged if no
+ *   mass is left), q'(x) <- 0 and q' is renormalised to the remaining mass.
+ * The walk ends at a leaf or when every child of the current node is
+ * rejected; the bonus token is then drawn from r by inversion: the smallest v
+ * with r(0) + ... + r(v) > coins[0].
+ *
+ *   draft_tokens  [B, N] int32; the root's entry is unused, the others must lie
+ *                 in [0, V).  The children of a node are taken to have been
+ *                 drawn without replacement from that node's draft_probs row.
+ *   target_logits [B, N, V] fp32, finite.
+ *   draft_probs   [B, N, V] fp32 draft probabilities q_u (each row sums to 1);
+ *                 only rows of visited nodes with children are read.
+ *   parent_idx    [B, N] int32 as for tree_build_ancestry.
+ *   coins         [B, N] fp32 uniforms in [0, 1): coins[b, c] decides child c,
+ *                 coins[b, 0] draws the bonus token.  The caller owns the
+ *                 random numbers.
+ *   temperature   > 0 and finite.
+ *   accepted      [B, max_depth + 1] int32 out: node ids root .. n*, then -1.
+ *   accept_len    [B] int32 out: number of accepted drafts.
+ *   bonus         [B] int32 out: the token drawn after n*.
+ *   status        [B] int32; only errors are written: TS_ERR_BAD_TREE for an
+ *                 invalid tree or a draft token outside [0, V) (row all -1,
+ *                 zeros), TS_ERR_SHAPE when the accepted path is longer than
+ *                 max_depth (row all -1, accept_len and bonus written),
+ *                 TS_ERR_TIMEOUT when an internal copy did not complete.
+ * fp32 arithmetic: decisions within fp32 rounding of a threshold may differ
+ * from an exact computation (the bonus by one token with mass at an
+ * inversion boundary).  Reads only the rows of the nodes the walk visits.
+ * No workspace.  Returns TS_ERR_NULL / TS_ERR_UNSUPPORTED (N outside
+ * [1, 256], V outside [1, 204800], B > 65535, max_depth < 0, temperature not
+ * positive and finite) / TS_ERR_CUDA.
+ */
+TS_API ts_status tree_verify_stochastic(const int32_t* draft_tokens, const float* target_logits,
+                                        const float* draft_probs, const int32_t* parent_idx, const float* coins,
+                                        int B, int N, int V, int max_depth, float temperature, int32_t* accepted,
+                                        int32_t* accept_len, int32_t* bonus, int32_t* status, ts_stream stream);
+
 /* Size of the library-owned scratch behind tree_verify_greedy_noalloc. */
 #define TS_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 

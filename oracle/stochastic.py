@@ -31,7 +31,8 @@ what distinct sibling tokens imply):
   * accepted = the path root .. n*, padded with -1 to max_depth + 1 entries;
     accept_len = depth(n*).  If depth(n*) > max_depth the row stays all -1,
     accept_len and bonus are still reported and the status is -2.  An invalid
-    tree gives status -3, an all -1 row and zeros.
+    tree, or a draft token outside [0, V) on a node other than the root, gives
+    status -3, an all -1 row and zeros.
 
 Each step is the single-draft speculative sampling step applied to the current
 residual, so the first token the walk emits (an accepted draft or the bonus)
@@ -83,7 +84,8 @@ def walk_stochastic(parent, draft, logits, q, coins, temperature: float, max_dep
     parent = [int(p) for p in parent]
     n = len(parent)
     path = np.full(max_depth + 1, -1, np.int32)
-    if not is_valid_tree(parent):
+    V = np.asarray(logits).shape[-1]
+    if not is_valid_tree(parent) or any(not (0 <= int(draft[c]) < V) for c in range(1, n)):
         out = (path, 0, 0, ERR_BAD_TREE, np.inf, np.inf)
         return out + (None,) if final else out
     kids = [[c for c in range(n) if parent[c] == u] for u in range(n)]

@@ -102,6 +102,9 @@ def test_hand_point_mass_draft_and_zero_coin():
 def test_invalid_tree_and_path_too_long():
     lg = _logits(P0, P0, P0)
     assert _walk([-1, 2, 0], [0, 1, 2], lg, [Q0] * 3, [0.5, 0.1, 0.1]) == ([-1] * 5, 0, 0, -3)
+    assert _walk([-1, 0, 0], [0, 1, 3], lg, [Q0] * 3, [0.5, 0.1, 0.1]) == ([-1] * 5, 0, 0, -3)
+    assert _walk([-1, 0, 0], [0, -1, 2], lg, [Q0] * 3, [0.5, 0.1, 0.1]) == ([-1] * 5, 0, 0, -3)
+    assert _walk([-1, 0, 0], [7, 1, 2], lg, [Q0] * 3, [0.5, 0.99, 0.99])[3] == 0   # the root's token is unused
     # chain 0 -> 1 -> 2 with one-hot-ish acceptance (coin 0) accepts both drafts
     assert _walk([-1, 0, 1], [0, 1, 1], lg, [Q0] * 3, [0.65, 0.0, 0.0])[:2] == ([0, 1, 2, -1, -1], 2)
     path, L, bonus, st = _walk([-1, 0, 1], [0, 1, 1], lg, [Q0] * 3, [0.65, 0.0, 0.0], max_depth=1)

@@ -21,7 +21,8 @@ from ._build import LIB as LIB_PATH
 __all__ = [
     "TreeSpecError", "lib", "ts_status_str", "tree_build_ancestry", "AttnParams", "attn_params",
     "tree_attn_workspace_size", "tree_attn_fwd", "tree_verify_workspace_size", "tree_verify_greedy",
-    "tree_verify_greedy_noalloc", "tree_commit_accepted", "NOALLOC_SCRATCH_BYTES", "STATUS",
+    "tree_verify_greedy_noalloc", "tree_commit_accepted", "tree_verify_stochastic", "NOALLOC_SCRATCH_BYTES",
+    "STATUS",
 ]
 
 STATUS = {
@@ -54,7 +55,7 @@ _LIB: Optional[ctypes.CDLL] = None
 # every symbol include/treespec.h declares
 EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_fwd",
            "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc",
-           "tree_commit_accepted")
+           "tree_commit_accepted", "tree_verify_stochastic")
 
 # TS_VERIFY_NOALLOC_SCRATCH_BYTES of treespec.h
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -85,6 +86,9 @@ def lib() -> ctypes.CDLL:
         L.tree_commit_accepted.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                            vp, vp, vp]
         L.tree_commit_accepted.restype = i32
+        L.tree_verify_stochastic.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp,
+                                             vp]
+        L.tree_verify_stochastic.restype = i32
         _LIB = L
     return _LIB
 
@@ -170,6 +174,17 @@ def tree_commit_accepted(k_tree, v_tree, accepted, accept_len, prefix_len, k_cac
                                       _p(k_cache), _p(v_cache), _p(block_table), B, N, Hkv, D, bs, nblk,
                                       block_table.shape[1], accepted.shape[1] - 1, _p(new_prefix_len), _p(status),
                                       _s(stream)), "tree_commit_accepted")
+
+
+def tree_verify_stochastic(draft_tokens, target_logits, draft_probs, parent_idx, coins, temperature: float,
+                           accepted, accept_len, bonus, status, stream=None) -> None:
+    """Rejection-sampling verification at the given temperature; max_depth is
+    accepted.shape[1] - 1.  coins [B, N] are the uniforms the walk consumes."""
+    B, N, V = target_logits.shape
+    _check(lib().tree_verify_stochastic(_p(draft_tokens), _p(target_logits), _p(draft_probs), _p(parent_idx),
+                                        _p(coins), B, N, V, accepted.shape[1] - 1, float(temperature),
+                                        _p(accepted), _p(accept_len), _p(bonus), _p(status), _s(stream)),
+           "tree_verify_stochastic")
 
 
 def tree_verify_greedy_noalloc(draft_tokens, target_logits, parent_idx, max_depth: int, accepted, accept_len, bonus,

@@ -98,8 +98,8 @@ AttnPlan plan_attn(const ts_attn_params* p) {
   return pl;
 }
 
-// The attention kernel's shared-memory opt-in, once per device (a host-side
-// attribute, so the first call should come before any stream capture).
+// The kernels' shared-memory opt-ins, once per device (host-side attributes,
+// so the first call should come before any stream capture).
 cudaError_t prepare_device() {
   static std::mutex mu;
   static bool done[64] = {};
@@ -110,6 +110,8 @@ cudaError_t prepare_device() {
   std::lock_guard<std::mutex> lock(mu);
   if (!done[dev]) {
     e = attn_tc_prepare();
+    if (e != cudaSuccess) return e;
+    e = stoch_prepare();
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
@@ -268,6 +270,38 @@ ts_status tree_commit_accepted(const void* k_tree, const void* v_tree, const int
   a.B = B; a.N = N; a.Hkv = Hkv; a.D = D; a.bs = block_size; a.num_blocks = num_blocks;
   a.max_blocks = max_blocks; a.max_depth = max_depth;
   return launch_commit(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+ts_status tree_verify_stochastic(const int32_t* draft_tokens, const float* target_logits, const float* draft_probs,
+                                 const int32_t* parent_idx, const float* coins, int B, int N, int V, int max_depth,
+                                 float temperature, int32_t* accepted, int32_t* accept_len, int32_t* bonus,
+                                 int32_t* status, ts_stream stream) {
+  if (!draft_tokens || !target_logits || !draft_probs || !parent_idx || !coins || !accepted || !accept_len ||
+      !bonus || !status)
+    return TS_ERR_NULL;
+  if (B < 1 || B > 65535 || N < 1 || N > MAX_NODES || V < 1 || V > STOCH_MAX_VOCAB || max_depth < 0)
+    return TS_ERR_UNSUPPORTED;
+  if (!(temperature > 0.f) || std::isinf(temperature)) return TS_ERR_UNSUPPORTED;
+  // the smallest cluster that keeps a slice within shared memory, grown while
+  // slices stay above STOCH_MIN_SLICE elements
+  int C = 1;
+  while (C < STOCH_MAX_CLUSTER && ceil_div(V, C) > STOCH_MIN_SLICE) C *= 2;
+  const int slice = (ceil_div(V, C) + 3) & ~3;
+  if (slice > STOCH_MAX_SLICE) return TS_ERR_UNSUPPORTED;
+  StochArgs a{};
+  a.draft = draft_tokens;
+  a.logits = target_logits;
+  a.q = draft_probs;
+  a.parent = parent_idx;
+  a.coins = coins;
+  a.B = B; a.N = N; a.V = V; a.max_depth = max_depth;
+  a.inv_temp_log2e = 1.4426950408889634f / temperature;
+  a.cluster = C;
+  a.slice = slice;
+  a.bulk = (V % 4 == 0) && aligned16(target_logits) && aligned16(draft_probs);
+  a.accepted = accepted; a.accept_len = accept_len; a.bonus = bonus; a.status = status;
+  if (prepare_device() != cudaSuccess) return TS_ERR_CUDA;
+  return launch_verify_stoch(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
 ts_status tree_verify_greedy_noalloc(const int32_t* draft_tokens, const float* target_logits,

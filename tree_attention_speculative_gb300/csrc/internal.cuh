@@ -145,4 +145,29 @@ struct CommitArgs {
 };
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
 
+// Stochastic verification: one cluster of `cluster` CTAs per sequence, CTA k
+// holding vocabulary slice [k*slice, (k+1)*slice) of the visited node's rows.
+struct StochArgs {
+  const int32_t* draft;
+  const float* logits;
+  const float* q;
+  const int32_t* parent;
+  const float* coins;
+  int B, N, V, max_depth;
+  float inv_temp_log2e;  // log2(e) / temperature
+  int cluster, slice;    // slice: elements per CTA, a multiple of 4
+  int bulk;              // rows start 16-byte aligned: slices arrive by bulk copy
+  int32_t* accepted;
+  int32_t* accept_len;
+  int32_t* bonus;
+  int32_t* status;
+};
+constexpr int STOCH_THREADS = 512;
+constexpr int STOCH_MAX_CLUSTER = 8;
+constexpr int STOCH_MIN_SLICE = 2048;                  // below this a smaller cluster is used
+constexpr int STOCH_MAX_SLICE = 25600;                 // 2 x 100 KB of shared memory per CTA
+constexpr int STOCH_MAX_VOCAB = STOCH_MAX_CLUSTER * STOCH_MAX_SLICE;
+cudaError_t stoch_prepare();
+cudaError_t launch_verify_stoch(const StochArgs& a, cudaStream_t s);
+
 }  // namespace ts

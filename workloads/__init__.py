@@ -422,6 +422,31 @@ def stochastic_inputs(seed: int, parent: np.ndarray, vocab: int, temperature: fl
     return StochasticInputs(draft=draft, logits=logits, q=q, coins=coins, temperature=float(temperature))
 
 
+def workload_trees(name: str, seed: int, batch: int = 64) -> np.ndarray:
+    """The [B, N] parent arrays of a named workload (the same draws its builder makes)."""
+    if name == "c1":
+        return tree_worked_example()[None, :]
+    g = rng(seed, "tree")
+    if name == "c2":
+        return tree_random_levels(g, 64, 6)[None, :]
+    if name == "c4":
+        return np.stack([tree_random_levels(g, 64, 8) for _ in range(batch)])
+    if name == "c5":
+        return np.stack([tree_random_levels(g, 192, 10) for _ in range(4)])
+    raise ValueError(f"{name} has no draft tokens to verify")
+
+
+SEEDS = {"c1": 20260001, "c2": 20260002, "c3": 20260003, "c4": 20260004, "c5": 20260005}
+VOCAB = {"c1": 1000, "c2": 128256, "c4": 128256, "c5": 128256}
+
+
+def stochastic_workload(name: str, temperature: float = 1.0, batch: int = 64, tag: str = "stoch"):
+    """Trees of a named workload with inputs for stochastic verification.
+    Returns (parent [B, N], StochasticInputs)."""
+    parent = workload_trees(name, SEEDS[name], batch=batch)
+    return parent, stochastic_inputs(SEEDS[name], parent, VOCAB[name], temperature=temperature, tag=tag)
+
+
 # The five workloads.  Seeds: 20260000 + k unless overridden.
 
 def c1(seed: int = 20260001, **extra) -> Case:
@@ -436,8 +461,7 @@ def c2(seed: int = 20260002, vocab: int = 128256, **extra) -> Case:
     4096-token prefix, a random 64-node tree of depth 6.  The workload lists no
     logits for this shape; the verification step here draws them over the
     Llama-3 vocabulary (128256) with a planted accepted length uniform in [0, 6]."""
-    g = rng(seed, "tree")
-    parent = tree_random_levels(g, 64, 6)
+    parent = workload_trees("c2", seed)[0]
     plant = int(rng(seed, "plant").integers(0, 7))
     case = build_case("c2", seed, parent, [4096], Hq=32, Hkv=8, D=128, bs=4096, permute=False,
                       vocab=vocab, plant_len=plant, **extra)
@@ -458,8 +482,7 @@ def c4(seed: int = 20260004, batch: int = 64, **extra) -> Case:
     """70B-shaped layer: batch 64, 64 q / 8 kv heads, head_dim 128, paged KV (block 16),
     prefix 8192; per-sequence random 64-node trees of depth 8; logits over 128256
     with planted accepted lengths uniform in [0, 8]."""
-    g = rng(seed, "tree")
-    parents = np.stack([tree_random_levels(g, 64, 8) for _ in range(batch)])
+    parents = workload_trees("c4", seed, batch=batch)
     plant = rng(seed, "plant").integers(0, 9, size=batch)
     return build_case("c4", seed, parents, [8192] * batch, Hq=64, Hkv=8, D=128, bs=16,
                       permute=True, vocab=128256, plant_len=plant, **extra)
@@ -470,8 +493,7 @@ def c5(seed: int = 20260005, prefix: int = 131072, **extra) -> Case:
     paged KV (block 64); a random 192-node tree of depth 10; 1% of key rows scaled by
     8; logits over 128256.  No accepted length is given for this shape; one uniform
     in [0, 10] is planted per sequence so that the walk is exercised."""
-    g = rng(seed, "tree")
-    parents = np.stack([tree_random_levels(g, 192, 10) for _ in range(4)])
+    parents = workload_trees("c5", seed)
     plant = rng(seed, "plant").integers(0, 11, size=4)
     return build_case("c5", seed, parents, [prefix] * 4, Hq=32, Hkv=8, D=128, bs=64,
                       permute=True, vocab=128256, plant_len=plant, hot_key_frac=0.01, **extra)
