@@ -645,11 +645,15 @@ def run_stochastic(args, world, rank, local):
     time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    w0 = time.time()
     e0.record()
     g.replay()
     e1.record()
     torch.cuda.synchronize()
-    clocks = sampler.stop()
+    w1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
     ms = e0.elapsed_time(e1) / args.steps
     # rows the walks had to read: every visited node's logits, plus its draft row when it has children
     nbytes = 0
@@ -664,12 +668,17 @@ def run_stochastic(args, world, rank, local):
     nbytes = nbytes / 2 + B * N * 4 * 3   # per call; + drafts, parents, coins
     pk = peaks()
     parent0, si0 = sets[0]
-    c0 = time.perf_counter()
-    reps = 0
-    while time.perf_counter() - c0 < 3.0 or reps < 1:
-        oracle.stochastic.verify_stochastic(si0.draft, si0.logits, si0.q, parent0, si0.coins, args.temperature, depth)
-        reps += 1
-    t_cpu = (time.perf_counter() - c0) / reps
+    cpu = None
+    if not args.no_cpu_baseline:
+        c0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - c0 < 3.0 or reps < 1:
+            oracle.stochastic.verify_stochastic(si0.draft, si0.logits, si0.q, parent0, si0.coins, args.temperature,
+                                                depth)
+            reps += 1
+        t_cpu = (time.perf_counter() - c0) / reps
+        cpu = {"value": B * N / t_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"the whole batch of this workload, {reps} repeats"}
     lens = np.concatenate([o["L"].cpu().numpy() for o in outs])
     line = {
         "metric": "stochastic tree verification: tree tokens verified/s", "value": B * N / (ms * 1e-3),
@@ -686,8 +695,7 @@ def run_stochastic(args, world, rank, local):
                      "note": "bytes = rows of the visited nodes only (the walk is sequential per sequence)"},
         "clocks": clocks,
         "gpu_launches": args.steps,
-        "cpu_baseline": {"value": B * N / t_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"the whole batch of this workload, {reps} repeats"},
+        "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
 
@@ -753,6 +761,8 @@ def main(argv=None):
         args.warmup = 3
     if args.steps <= 0:
         args.steps = default_steps(args.workload) if args.impl == "ours" else 3
+        if args.impl == "ours" and args.part == "stochastic":
+            args.steps = 3000   # about 0.25 s of timed work, long enough for the clock samples
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -290,9 +290,11 @@ TS_API ts_status tree_commit_accepted(const void* k_tree, const void* v_tree, co
  * fp32 arithmetic: decisions within fp32 rounding of a threshold may differ
  * from an exact computation (the bonus by one token with mass at an
  * inversion boundary).  Reads only the rows of the nodes the walk visits.
- * No workspace.  Returns TS_ERR_NULL / TS_ERR_UNSUPPORTED (N outside
- * [1, 256], V outside [1, 204800], B > 65535, max_depth < 0, temperature not
- * positive and finite) / TS_ERR_CUDA.
+ * No workspace.  The first call on a device sets kernel attributes; make it
+ * outside any stream capture.  Returns TS_ERR_NULL / TS_ERR_UNSUPPORTED (N
+ * outside [1, 256], V outside [1, 409600] (204800 on GPUs without 16-CTA
+ * clusters), B > 65535, max_depth < 0, temperature not positive and finite) /
+ * TS_ERR_CUDA.
  */
 TS_API ts_status tree_verify_stochastic(const int32_t* draft_tokens, const float* target_logits,
                                         const float* draft_probs, const int32_t* parent_idx, const float* coins,

@@ -98,11 +98,13 @@ AttnPlan plan_attn(const ts_attn_params* p) {
   return pl;
 }
 
-// The kernels' shared-memory opt-ins, once per device (host-side attributes,
-// so the first call should come before any stream capture).
-cudaError_t prepare_device() {
+// The kernels' opt-ins, once per device (host-side attributes, so the first
+// call should come before any stream capture).  Also reports the largest
+// cluster the stochastic verifier may use on this device.
+cudaError_t prepare_device(int* stoch_max_cluster = nullptr) {
   static std::mutex mu;
   static bool done[64] = {};
+  static int max_cluster[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -111,10 +113,11 @@ cudaError_t prepare_device() {
   if (!done[dev]) {
     e = attn_tc_prepare();
     if (e != cudaSuccess) return e;
-    e = stoch_prepare();
+    e = stoch_prepare(&max_cluster[dev]);
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
+  if (stoch_max_cluster) *stoch_max_cluster = max_cluster[dev];
   return cudaSuccess;
 }
 
@@ -279,13 +282,15 @@ ts_status tree_verify_stochastic(const int32_t* draft_tokens, const float* targe
   if (!draft_tokens || !target_logits || !draft_probs || !parent_idx || !coins || !accepted || !accept_len ||
       !bonus || !status)
     return TS_ERR_NULL;
-  if (B < 1 || B > 65535 || N < 1 || N > MAX_NODES || V < 1 || V > STOCH_MAX_VOCAB || max_depth < 0)
+  if (B < 1 || B > 65535 || N < 1 || N > MAX_NODES || V < 1 || V > STOCH_MAX_CLUSTER * STOCH_MAX_SLICE ||
+      max_depth < 0)
     return TS_ERR_UNSUPPORTED;
   if (!(temperature > 0.f) || std::isinf(temperature)) return TS_ERR_UNSUPPORTED;
-  // the smallest cluster that keeps a slice within shared memory, grown while
-  // slices stay above STOCH_MIN_SLICE elements
+  int max_cluster = STOCH_PORTABLE_CLUSTER;
+  if (prepare_device(&max_cluster) != cudaSuccess) return TS_ERR_CUDA;
+  // the cluster doubles until a slice holds at most STOCH_TARGET_SLICE elements
   int C = 1;
-  while (C < STOCH_MAX_CLUSTER && ceil_div(V, C) > STOCH_MIN_SLICE) C *= 2;
+  while (C < max_cluster && ceil_div(V, C) > STOCH_TARGET_SLICE) C *= 2;
   const int slice = (ceil_div(V, C) + 3) & ~3;
   if (slice > STOCH_MAX_SLICE) return TS_ERR_UNSUPPORTED;
   StochArgs a{};
@@ -300,7 +305,6 @@ ts_status tree_verify_stochastic(const int32_t* draft_tokens, const float* targe
   a.slice = slice;
   a.bulk = (V % 4 == 0) && aligned16(target_logits) && aligned16(draft_probs);
   a.accepted = accepted; a.accept_len = accept_len; a.bonus = bonus; a.status = status;
-  if (prepare_device() != cudaSuccess) return TS_ERR_CUDA;
   return launch_verify_stoch(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 

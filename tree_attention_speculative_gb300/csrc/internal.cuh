@@ -162,12 +162,12 @@ struct StochArgs {
   int32_t* bonus;
   int32_t* status;
 };
-constexpr int STOCH_THREADS = 512;
-constexpr int STOCH_MAX_CLUSTER = 8;
-constexpr int STOCH_MIN_SLICE = 2048;                  // below this a smaller cluster is used
+constexpr int STOCH_THREADS = 256;
+constexpr int STOCH_MAX_CLUSTER = 16;                  // where the GPU allows non-portable clusters
+constexpr int STOCH_PORTABLE_CLUSTER = 8;
+constexpr int STOCH_TARGET_SLICE = 8192;               // the cluster grows until a slice is this small
 constexpr int STOCH_MAX_SLICE = 25600;                 // 2 x 100 KB of shared memory per CTA
-constexpr int STOCH_MAX_VOCAB = STOCH_MAX_CLUSTER * STOCH_MAX_SLICE;
-cudaError_t stoch_prepare();
+cudaError_t stoch_prepare(int* max_cluster);
 cudaError_t launch_verify_stoch(const StochArgs& a, cudaStream_t s);
 
 }  // namespace ts

@@ -13,23 +13,25 @@
 // (or u is a leaf) the bonus token is drawn from r by inversion with coins[0].
 //
 // Design.  The walk only ever needs the rows of the nodes it visits, so it is
-// run lazily, one sequence per thread-block cluster of C CTAs.  CTA k of the
-// cluster owns vocabulary slice [k*S, (k+1)*S) and holds, in shared memory, its
-// slice of the visited node's target logits and draft probabilities (brought
-// in by one bulk copy each).  Per visited node:
-//   1. local max and sum of exp((l - max)/T), one cluster exchange -> the
-//      global normaliser and a rescale factor per CTA;
-//   2. every CTA gathers r(x), q'(x) of the node's children tokens from their
-//      owners over distributed shared memory, so each acceptance test is local;
-//   3. each rejection costs one slice pass (sum of the residual) and one
-//      exchange, then an in-place update of the slice;
-//   4. the bonus draw locates the owning CTA from the per-CTA masses and that
-//      CTA scans its slice.
+// run lazily, one sequence per thread-block cluster of C CTAs (C up to 16 where
+// the GPU allows non-portable clusters, else 8).  CTA k of the cluster owns
+// vocabulary slice [k*S, (k+1)*S) and holds, in shared memory, its slice of the
+// visited node's target logits and draft probabilities (one bulk copy each).
+// Per visited node:
+//   1. the slice's (max, sum of exp((l - max)/T)) in one pass; one cluster
+//      exchange gives the global normaliser and a rescale factor per CTA;
+//   2. every CTA reads the node's children tokens' logits and draft
+//      probabilities from global memory itself (while the slices land) and
+//      rescales them as their owner would, so each acceptance test is local;
+//   3. each rejection costs one slice pass (sum of the residual), one
+//      exchange and an in-place update of the slice;
+//   4. the bonus draw locates the owning CTA from the per-CTA masses, and that
+//      CTA scans its slice, each warp a contiguous run read lane by lane.
 // Every CTA takes every decision itself from exchanged values read in the same
 // order with the same fp32 operations, so the CTAs of a cluster never diverge.
-// Reuse of a buffer or an exchange slot is ordered by the cluster barriers:
-// records alternate between two slots, and a CTA overwrites its slices only
-// after every CTA has signalled that its gathers for the node are done.
+// An exchange is one 16-byte record per CTA pushed into every peer's shared
+// memory (st.async, completing on the receiver's mbarrier): no cluster-wide
+// barrier on the walk, and no CTA ever reads another's slices.
 #include <float.h>
 
 #include "internal.cuh"
@@ -57,17 +59,6 @@ __device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ int ld_peer_s32(uint32_t addr) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 // One bulk copy global -> this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -76,28 +67,30 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-// What each CTA publishes at an exchange.
-struct Rec {
-  float a, b;
-  int err, pad;
-};
-
 struct Shared {
   int parent[MAX_NODES];
   int draft[MAX_NODES];
-  int kid_start[MAX_NODES + 1];
-  int kid_cnt[MAX_NODES];
-  int kids[MAX_NODES];
+  int has_kids[MAX_NODES];
+  int kid_list[MAX_NODES];  // the current node's children, in index order
   int path[MAX_NODES];
-  float cr[MAX_NODES];  // residual mass r(x) * S of the current node's children tokens
-  float cq[MAX_NODES];  // draft probability q(x) of the same tokens (0 once excluded)
-  Rec rec[2];           // exchange slots, alternating
-  Rec all[STOCH_MAX_CLUSTER];
-  float fac[STOCH_MAX_CLUSTER];  // per-CTA rescale of the slice values
-  float tot[STOCH_MAX_CLUSTER];  // per-CTA mass of the current residual
-  float red[ST_WARPS + 1];
+  float cl[MAX_NODES];  // target logit of each child's token at the current node
+  float cr[MAX_NODES];  // its residual mass r(x) * S
+  float cq[MAX_NODES];  // its draft probability q(x) (0 once excluded)
+  float coin[MAX_NODES];
+  float4 xrec[2][STOCH_MAX_CLUSTER];  // exchange records, one slot per sending CTA, two exchanges in flight
+  float4 all[STOCH_MAX_CLUSTER];      // the last exchange's records, copied out of the slot
+  float fac[STOCH_MAX_CLUSTER];       // per-CTA rescale of the slice values
+  float tot[STOCH_MAX_CLUSTER];       // per-CTA mass of the current residual
+  float red[2 * ST_WARPS];
+  float wm[ST_WARPS], ws[ST_WARPS];   // each warp's (max, sum) from the normaliser pass
+  float wmass[ST_WARPS];              // each warp's residual mass once the slice holds residuals
+  float wpend[ST_WARPS];              // the same for a residual being computed
+  float S;
+  int nk;
+  int xerr;  // some CTA of the cluster reported an error at the last exchange
   int claim;
-  uint64_t bar;
+  uint64_t bar;      // the slices' bulk copies
+  uint64_t xbar[2];  // arrival of every CTA's record for an exchange slot
 };
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -105,79 +98,108 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-template <bool MAX>
-__device__ float block_reduce(float v, float* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = MAX ? warp_max(v) : warp_sum(v);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    float w = lane < ST_WARPS ? red[lane] : (MAX ? -FLT_MAX : 0.f);
-    w = MAX ? warp_max(w) : warp_sum(w);
-    if (lane == 0) red[ST_WARPS] = w;
-  }
-  __syncthreads();
-  return red[ST_WARPS];
+// exp((l - m) / T) as 2^((l - m) * log2(e) / T), with explicit roundings: every
+// CTA that evaluates it for the same (l, m) gets the same bits.
+__device__ __forceinline__ float unnorm_p(float l, float m, float kT) { return ex2(__fmul_rn(__fsub_rn(l, m), kT)); }
+
+// The residual of one element: max(rho - k * q, 0), rho already in the common
+// scale; explicit roundings for the same reason.
+__device__ __forceinline__ float residual(float rho, float k, float q) { return fmaxf(__fmaf_rn(-k, q, rho), 0.f); }
+
+// Merge two (max, sum of 2^((x - max) kT)) pairs.
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float kT) {
+  const float mn = fmaxf(m, m2);
+  s = __fmul_rn(s, unnorm_p(m, mn, kT)) + __fmul_rn(s2, unnorm_p(m2, mn, kT));
+  m = mn;
 }
 
-// The residual update of one element: max(f * rho - k * q, 0), written with
-// explicit roundings so that every CTA that evaluates it for the same inputs
-// gets the same bits.
-__device__ __forceinline__ float residual(float rho_scaled, float k, float q) {
-  return fmaxf(__fmaf_rn(-k, q, rho_scaled), 0.f);
+// Store 16 bytes into a peer CTA's shared memory; completes on the peer's mbarrier.
+__device__ __forceinline__ void st_async16(uint32_t dst, float4 v, uint32_t peer_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+               "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+               "r"(__float_as_uint(v.w)), "r"(peer_bar)
+               : "memory");
 }
 
-// Exchange: publish (a, b, err) and read every CTA's record, in rank order, into sh.all.
-__device__ void exchange(Shared& sh, int& xcnt, bool& pending, int C, float a, float b, int err) {
-  if (pending) {
-    cl_wait();
-    pending = false;
-  }
-  Rec* slot = &sh.rec[xcnt & 1];
-  if (threadIdx.x == 0) *slot = Rec{a, b, err, 0};
-  cl_arrive();
-  cl_wait();
-  if ((int)threadIdx.x < C) {
-    const uint32_t base = peer_addr(slot, threadIdx.x);
-    sh.all[threadIdx.x] = Rec{ld_peer_f32(base), ld_peer_f32(base + 4), ld_peer_s32(base + 8), 0};
-  }
-  __syncthreads();
-  ++xcnt;
-}
+// The current value of slice element x: while the slice still holds raw
+// logits, the unnormalised target probability rescaled to the common scale;
+// after the first residual update, the residual itself (scale 1).
+struct SliceVal {
+  float m, kT, f;
+  bool raw;
+  __device__ __forceinline__ float operator()(float x) const { return __fmul_rn(f, raw ? unnorm_p(x, m, kT) : x); }
+};
 
-__global__ void __launch_bounds__(STOCH_THREADS, 1) k_verify_stoch(StochArgs a) {
+__global__ void __launch_bounds__(STOCH_THREADS, 2) k_verify_stoch(StochArgs a) {
   extern __shared__ __align__(128) float dyn[];
   __shared__ Shared sh;
-  float* bufL = dyn;             // slice of the node's target logits, then of the residual
-  float* bufQ = dyn + a.slice;   // slice of the node's draft probabilities
+  float* bufL = dyn;            // slice of the node's target logits, then of the residual
+  float* bufQ = dyn + a.slice;  // slice of the node's draft probabilities
   const int C = a.cluster;
   const int rank = (int)cluster_rank();
   const int b = blockIdx.y;
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int N = a.N, V = a.V;
   const int v0 = rank * a.slice;
   const int len = max(0, min(a.slice, V - v0));
+  // The slice as float4 (padded to a multiple of 4 with tokens of no mass);
+  // warp w walks the contiguous run [wlo, whi) of it, lane by lane.
+  const int len4 = (len + 3) >> 2;
+  const int run4 = (len4 + ST_WARPS - 1) / ST_WARPS;
+  const int wlo = min(len4, warp * run4), whi = min(len4, wlo + run4);
+  float4* L4 = reinterpret_cast<float4*>(bufL);
+  const float4* Q4 = reinterpret_cast<const float4*>(bufQ);
+  const float kT = a.inv_temp_log2e;
 
   if (tid == 0) {
     mbar_init(&sh.bar, 1);
+    mbar_init(&sh.xbar[0], 1);
+    mbar_init(&sh.xbar[1], 1);
     fence_barrier_init();
   }
   __syncthreads();
+  cl_arrive();  // this CTA's exchange barriers exist; waited on before the first record is sent
   pdl_wait();
   pdl_trigger();
 
-  // Bring in one node's slices (logits always, draft probabilities if it has children).
+  int err = 0;
+  // Exchange: publish (a, b, err) to every CTA of the cluster and collect
+  // everyone's record, in rank order, into sh.all.  Records go straight into
+  // the peers' slots (st.async), completing on the peers' slot barrier, so no
+  // cluster-wide barrier is needed.  Slot s is rewritten by a peer only after
+  // that peer has this CTA's record of the next exchange, which is sent after
+  // this CTA copied slot s out.
+  int xcnt = 0;
+  auto exchange = [&](float va, float vb, int e) {
+    const int s = xcnt & 1;
+    if (xcnt == 0) cl_wait();
+    if (tid == 0) mbar_arrive_expect_tx(&sh.xbar[s], (uint32_t)C * 16u);
+    if (tid < C) {
+      const float4 rec = make_float4(va, vb, __int_as_float(e), 0.f);
+      st_async16(peer_addr(&sh.xrec[s][rank], tid), rec, peer_addr(&sh.xbar[s], tid));
+    }
+    const bool ok = mbar_wait(&sh.xbar[s], (uint32_t)(xcnt >> 1) & 1u, WAIT_NS);
+    if (tid < C) sh.all[tid] = sh.xrec[s][tid];
+    if (!__syncthreads_and(ok)) err = 1;
+    ++xcnt;
+  };
+
+  // Bring in one node's slices (logits always, draft probabilities if it has
+  // children).  Lane 0 of warp 1 issues the bulk copies, so warp 0 is free to
+  // fetch the children's values meanwhile.
   uint32_t phase = 0;
   auto issue = [&](int u, bool with_q) {
     const size_t row = ((size_t)b * N + u) * (size_t)V + v0;
     if (a.bulk) {
-      if (tid == 0) {
+      if (tid == 32) {
         // order this CTA's earlier generic-proxy accesses of the slices before the copy's writes
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         const uint32_t bytes = (uint32_t)len * 4u;
@@ -188,9 +210,9 @@ __global__ void __launch_bounds__(STOCH_THREADS, 1) k_verify_stoch(StochArgs a) 
         }
       }
     } else {
-      for (int i = tid; i < len; i += STOCH_THREADS) {
-        bufL[i] = a.logits[row + i];
-        if (with_q) bufQ[i] = a.q[row + i];
+      for (int i = tid; i < 4 * len4; i += STOCH_THREADS) {
+        bufL[i] = i < len ? a.logits[row + i] : -FLT_MAX;
+        if (with_q) bufQ[i] = i < len ? a.q[row + i] : 0.f;
       }
     }
   };
@@ -213,7 +235,7 @@ __global__ void __launch_bounds__(STOCH_THREADS, 1) k_verify_stoch(StochArgs a) 
     const int d = a.draft[(size_t)b * N + i];
     sh.parent[i] = p;
     sh.draft[i] = d;
-    sh.kid_cnt[i] = 0;
+    sh.has_kids[i] = 0;
     bad |= (i == 0) ? (p != -1) : (p < 0 || p >= i || d < 0 || d >= V);
   }
   if (__syncthreads_or(bad)) {
@@ -225,125 +247,169 @@ __global__ void __launch_bounds__(STOCH_THREADS, 1) k_verify_stoch(StochArgs a) 
       a.bonus[b] = 0;
       a.status[b] = TS_ERR_BAD_TREE;
     }
+    cl_wait();
     return;  // no distributed shared memory was touched
   }
-  // children lists in index order
-  for (int c = 1 + tid; c < N; c += STOCH_THREADS) atomicAdd(&sh.kid_cnt[sh.parent[c]], 1);
-  __syncthreads();
-  if (tid == 0) {
-    int s = 0;
-    for (int u = 0; u < N; ++u) {
-      sh.kid_start[u] = s;
-      s += sh.kid_cnt[u];
-    }
-    sh.kid_start[N] = s;
-    sh.path[0] = 0;
-  }
-  __syncthreads();
-  for (int c = 1 + tid; c < N; c += STOCH_THREADS) {
-    const int p = sh.parent[c];
-    int r = 0;
-    for (int j = 1; j < c; ++j) r += (sh.parent[j] == p);
-    sh.kids[sh.kid_start[p] + r] = c;
-  }
-  __syncthreads();
+  for (int c = 1 + tid; c < N; c += STOCH_THREADS) sh.has_kids[sh.parent[c]] = 1;
+  if (tid == 0) sh.path[0] = 0;
 
-  const float kT = a.inv_temp_log2e;
-  int xcnt = 0;
-  bool pending = false;  // a "done reading peers' slices" arrive not yet waited on
-  int err = 0;
   int depth = 0;
   int u = 0;
   bool first = true;
 
   while (true) {
-    const int nk = sh.kid_cnt[u];
-    if (!first) {
-      if (pending) {
-        cl_wait();
-        pending = false;
-      }
-      issue(u, nk > 0);
-    }
+    __syncthreads();  // the previous node's reads of the slices and child arrays are done
+    const size_t urow = ((size_t)b * N + u) * (size_t)V;
+    // No CTA reads another's slices, so the next node's copy may start at once.
+    if (!first) issue(u, sh.has_kids[u] != 0);
     first = false;
+    // u's children in index order (warp ballots over the parent array)
+    if (warp == 0) {
+      int cnt = 0;
+      for (int base = (u + 1) & ~31; base < N; base += 32) {
+        const int c = base + lane;
+        const bool kid = c > u && c < N && sh.parent[c] == u;
+        const unsigned bal = __ballot_sync(0xffffffffu, kid);
+        if (kid) sh.kid_list[cnt + __popc(bal & ((1u << lane) - 1u))] = c;
+        cnt += __popc(bal);
+      }
+      if (lane == 0) sh.nk = cnt;
+    }
+    __syncthreads();
+    const int k0 = 0;
+    const int nk = sh.nk;
+    // the children tokens' own values and coins, straight from global memory while the slices land
+    for (int j = tid; j < nk; j += STOCH_THREADS) {
+      const int c = sh.kid_list[k0 + j];
+      const int x = sh.draft[c];
+      sh.cl[j] = a.logits[urow + x];
+      sh.cq[j] = a.q[urow + x];
+      sh.coin[j] = a.coins[(size_t)b * N + c];
+    }
     if (!land()) err = 1;
 
-    // 1. normaliser of softmax(l / T) over the vocabulary
-    float m = -FLT_MAX;
-    for (int i = tid; i < len; i += STOCH_THREADS) m = fmaxf(m, bufL[i]);
-    const float m_me = block_reduce<true>(m, sh.red);
-    float s = 0.f;
-    for (int i = tid; i < len; i += STOCH_THREADS) {
-      const float e = exp2f((bufL[i] - m_me) * kT);
-      bufL[i] = e;
-      s += e;
+    // 1. normaliser of softmax(l / T): (max, sum of 2^((l - max) kT)) in one
+    //    pass, eight float4 per thread at a time held in registers
+    float m = -FLT_MAX, s = 0.f;
+    for (int i0 = wlo + lane; i0 < whi; i0 += 8 * 32) {
+      float4 l[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = i0 + 32 * k;
+        l[k] = i < whi ? L4[i] : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+      }
+      float mx = m;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fmaxf(fmaxf(l[k].x, l[k].y), fmaxf(l[k].z, l[k].w)));
+      float part[4] = {__fmul_rn(s, unnorm_p(m, mx, kT)), 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        part[0] += unnorm_p(l[k].x, mx, kT);
+        part[1] += unnorm_p(l[k].y, mx, kT);
+        part[2] += unnorm_p(l[k].z, mx, kT);
+        part[3] += unnorm_p(l[k].w, mx, kT);
+      }
+      s = (part[0] + part[1]) + (part[2] + part[3]);
+      m = mx;
     }
-    const float s_me = block_reduce<false>(s, sh.red);
-    exchange(sh, xcnt, pending, C, len > 0 ? m_me : -FLT_MAX, s_me, err);
-    int err_any = 0;
-    float gm = -FLT_MAX;
-    for (int r = 0; r < C; ++r) {
-      err_any |= sh.all[r].err;
-      gm = fmaxf(gm, sh.all[r].a);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      merge_ms(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o), kT);
+    if (lane == 0) {
+      sh.wm[warp] = m;
+      sh.ws[warp] = s;
     }
-    if (err_any) {
+    __syncthreads();
+    // every warp merges the warps' pairs in the same order
+    m = lane < ST_WARPS ? sh.wm[lane] : -FLT_MAX;
+    s = lane < ST_WARPS ? sh.ws[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      merge_ms(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o), kT);
+    const float m_me = m;
+    exchange(len > 0 ? m_me : -FLT_MAX, s, err);
+    // warp 0 folds the records: global max, per-CTA factor and mass, total
+    if (warp == 0) {
+      const float4 rec = lane < C ? sh.all[lane] : make_float4(-FLT_MAX, 0.f, 0.f, 0.f);
+      const int e_any = __any_sync(0xffffffffu, lane < C && __float_as_int(rec.z) != 0);
+      float gm = rec.x;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+      const float f = unnorm_p(rec.x, gm, kT);
+      const float t = __fmul_rn(f, rec.y);
+      if (lane < C) {
+        sh.fac[lane] = f;
+        sh.tot[lane] = t;
+      }
+      __syncwarp();
+      float tv[STOCH_MAX_CLUSTER];
+#pragma unroll
+      for (int r = 0; r < STOCH_MAX_CLUSTER; ++r) tv[r] = __shfl_sync(0xffffffffu, t, r);
+      float S0 = 0.f;  // sequential, in rank order, as the bonus draw adds them up
+#pragma unroll
+      for (int r = 0; r < STOCH_MAX_CLUSTER; ++r)
+        if (r < C) S0 = __fadd_rn(S0, tv[r]);
+      if (lane == 0) {
+        sh.S = S0;
+        sh.xerr = e_any;
+      }
+      // 2. the children tokens' target mass in the common scale (what their owner computes)
+      for (int j = lane; j < nk; j += 32) {
+        const int o = sh.draft[sh.kid_list[k0 + j]] / a.slice;
+        sh.cr[j] = __fmul_rn(sh.fac[o], unnorm_p(sh.cl[j], sh.all[o].x, kT));
+      }
+    }
+    __syncthreads();
+    if (sh.xerr) {
       err = 1;
       break;
     }
-    float S = 0.f;
-    float fac_me = 1.f;
-    if (tid < C) {
-      const float f = exp2f((sh.all[tid].a - gm) * kT);
-      sh.fac[tid] = f;
-      sh.tot[tid] = __fmul_rn(f, sh.all[tid].b);
-    }
-    __syncthreads();
-    for (int r = 0; r < C; ++r) S = __fadd_rn(S, sh.tot[r]);
-    fac_me = sh.fac[rank];
-
-    // 2. gather the children tokens' values from their owners
-    const int k0 = sh.kid_start[u];
-    for (int j = tid; j < nk; j += STOCH_THREADS) {
-      const int x = sh.draft[sh.kids[k0 + j]];
-      const int o = x / a.slice;
-      const int off = x - o * a.slice;
-      sh.cr[j] = __fmul_rn(sh.fac[o], ld_peer_f32(peer_addr(bufL + off, o)));
-      sh.cq[j] = ld_peer_f32(peer_addr(bufQ + off, o));
-    }
-    cl_arrive();  // this CTA is done reading its peers' slices for node u
-    pending = true;
-    __syncthreads();
+    float S = sh.S;
+    SliceVal val{m_me, kT, sh.fac[rank], true};
 
     // 3. try the children in index order
     float Qm = 1.f;  // draft mass left after excluding rejected tokens
     int next = -1;
     for (int j = 0; j < nk; ++j) {
-      const int c = sh.kids[k0 + j];
+      const int c = sh.kid_list[k0 + j];
       const int x = sh.draft[c];
-      const float coin = a.coins[(size_t)b * N + c];
       const float rx = sh.cr[j], qx = sh.cq[j];
-      const bool acc = Qm > 0.f ? (__fmul_rn(__fmul_rn(coin, qx), S) < __fmul_rn(rx, Qm)) : (rx > 0.f);
+      const bool acc = Qm > 0.f ? (__fmul_rn(__fmul_rn(sh.coin[j], qx), S) < __fmul_rn(rx, Qm)) : (rx > 0.f);
       if (acc) {
         next = c;
         break;
       }
       if (Qm > 0.f) {
-        // residual: r <- max(r - q', 0), in the slice's own scale: rho <- max(f*rho - (S/Qm)*q, 0)
+        // residual: r <- max(r - q', 0), in the common scale: rho <- max(rho - (S/Qm) q, 0)
         const float kq = __fdiv_rn(S, Qm);
         float t = 0.f;
-        for (int i = tid; i < len; i += STOCH_THREADS) t += residual(__fmul_rn(fac_me, bufL[i]), kq, bufQ[i]);
-        const float t_me = block_reduce<false>(t, sh.red);
-        exchange(sh, xcnt, pending, C, t_me, 0.f, 0);
+        for (int i = wlo + lane; i < whi; i += 32) {
+          const float4 l = L4[i], q = Q4[i];
+          t += (residual(val(l.x), kq, q.x) + residual(val(l.y), kq, q.y)) +
+               (residual(val(l.z), kq, q.z) + residual(val(l.w), kq, q.w));
+        }
+        t = warp_sum(t);
+        if (lane == 0) sh.wpend[warp] = t;
+        __syncthreads();
+        const float t_me = warp_sum(lane < ST_WARPS ? sh.wpend[lane] : 0.f);
+        exchange(t_me, 0.f, 0);
         float S2 = 0.f;
-        for (int r = 0; r < C; ++r) S2 = __fadd_rn(S2, sh.all[r].a);
+        for (int r = 0; r < C; ++r) S2 = __fadd_rn(S2, sh.all[r].x);
+        if (err) break;
         if (S2 > 0.f) {
-          for (int i = tid; i < len; i += STOCH_THREADS) bufL[i] = residual(__fmul_rn(fac_me, bufL[i]), kq, bufQ[i]);
+          for (int i = wlo + lane; i < whi; i += 32) {
+            const float4 l = L4[i], q = Q4[i];
+            L4[i] = make_float4(residual(val(l.x), kq, q.x), residual(val(l.y), kq, q.y),
+                                residual(val(l.z), kq, q.z), residual(val(l.w), kq, q.w));
+          }
           for (int jj = j + 1 + tid; jj < nk; jj += STOCH_THREADS) sh.cr[jj] = residual(sh.cr[jj], kq, sh.cq[jj]);
           if (tid < C) {
             sh.fac[tid] = 1.f;
-            sh.tot[tid] = sh.all[tid].a;
+            sh.tot[tid] = sh.all[tid].x;
           }
-          fac_me = 1.f;
+          if (tid < ST_WARPS) sh.wmass[tid] = sh.wpend[tid];
+          val.raw = false;
+          val.f = 1.f;
           S = S2;
         }
         __syncthreads();  // every thread is done with bufQ before x's entry is cleared
@@ -353,14 +419,15 @@ __global__ void __launch_bounds__(STOCH_THREADS, 1) k_verify_stoch(StochArgs a) 
       const int o = x / a.slice;
       if (o == rank && tid == 0) bufQ[x - o * a.slice] = 0.f;
       for (int jj = j + 1 + tid; jj < nk; jj += STOCH_THREADS)
-        if (sh.draft[sh.kids[k0 + jj]] == x) sh.cq[jj] = 0.f;
+        if (sh.draft[sh.kid_list[k0 + jj]] == x) sh.cq[jj] = 0.f;
       __syncthreads();
     }
+    if (err) break;
     if (next >= 0) {
       ++depth;
       if (tid == 0) sh.path[depth] = next;
       u = next;
-      continue;  // the next iteration waits on the arrive above before reusing the slices
+      continue;
     }
 
     // 4. bonus token: smallest v with cumulative residual mass > coins[0] * S
@@ -385,58 +452,79 @@ __global__ void __launch_bounds__(STOCH_THREADS, 1) k_verify_stoch(StochArgs a) 
       last_positive = true;
     }
     if (owner == rank) {
-      const float tt = __fsub_rn(t_all, base);
-      const int per = (len + STOCH_THREADS - 1) / STOCH_THREADS;
-      const int lo = min(len, tid * per), hi = min(len, lo + per);
-      float mine = 0.f;
-      for (int i = lo; i < hi; ++i) mine = __fadd_rn(mine, __fmul_rn(fac_me, bufL[i]));
-      // exclusive scan of the per-thread sums
-      const int lane = tid & 31, warp = tid >> 5;
-      float inc = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
+      // each warp's mass is known from the last pass over the slice
+      auto wmass = [&](int w) -> float {
+        return val.raw ? __fmul_rn(val.f, __fmul_rn(sh.ws[w], unnorm_p(sh.wm[w], m_me, kT))) : sh.wmass[w];
+      };
+      // the warp whose run holds the target: the first whose running total passes it
+      const float t_me = __fsub_rn(t_all, base);
+      int tw = -1;
+      float excl = 0.f;
+      for (int w = 0; w < ST_WARPS && tw < 0; ++w) {
+        const float nx = __fadd_rn(excl, wmass(w));
+        if (nx > t_me) tw = w;
+        else excl = nx;
       }
-      if (lane == 31) sh.red[warp] = inc;
       if (tid == 0) sh.claim = INT_MAX;
       __syncthreads();
-      if (warp == 0) {
-        float w = lane < ST_WARPS ? sh.red[lane] : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, w, o);
-          if (lane >= o) w += y;
-        }
-        if (lane < ST_WARPS) sh.red[lane] = w - sh.red[lane];  // exclusive prefix of the warps
-      }
-      __syncthreads();
-      const float excl = sh.red[warp] + (inc - mine);
-      // A thread whose range ends beyond the target claims the first token in
-      // it where the running mass passes the target; the smallest claim wins,
-      // so a rounding gap between two ranges only moves the draw to the
-      // neighbouring token with mass.
-      int found = -1;
-      if (!last_positive && lo < hi) {
-        const float d = __fsub_rn(tt, excl);
-        if (d < mine) {
-          float acc = 0.f;
-          for (int i = lo; i < hi; ++i) {
-            const float w = __fmul_rn(fac_me, bufL[i]);
-            acc = __fadd_rn(acc, w);
-            if (acc > d && w > 0.f) {
-              found = i;
-              break;
-            }
+      // That warp finds the lane whose group of the run holds the target (each
+      // lane sums a contiguous group of float4, reading it in an order rotated
+      // by the lane so that the lanes hit different banks); then the warp walks
+      // that group one token per lane to the first token with mass where the
+      // running sum passes the target.  If rounding leaves the target beyond
+      // the last group, the run's last token with mass is taken.
+      if (!last_positive && warp == tw && wlo < whi) {
+        const float d = __fsub_rn(t_me, excl);
+        const int g4 = (whi - wlo + 31) >> 5;  // float4 per lane group
+        const int glo = min(whi, wlo + lane * g4), ghi = min(whi, glo + g4);
+        const int rot = lane % g4;
+        float gs = 0.f;
+        for (int k = 0; k < g4; ++k) {
+          int idx = k + rot;
+          if (idx >= g4) idx -= g4;
+          const int i = glo + idx;
+          if (i < ghi) {
+            const float4 l = L4[i];
+            gs += (val(l.x) + val(l.y)) + (val(l.z) + val(l.w));
           }
         }
+        float inc = gs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, gs > 0.f && inc > d);
+        const unsigned any = __ballot_sync(0xffffffffu, gs > 0.f);
+        // the group that passes the target, else the run's last group with mass
+        const int L = hit ? __ffs(hit) - 1 : (any ? 31 - __clz(any) : -1);
+        if (L >= 0) {
+          float run = __shfl_sync(0xffffffffu, inc - gs, L);
+          const int e_lo = 4 * __shfl_sync(0xffffffffu, glo, L), e_hi = 4 * __shfl_sync(0xffffffffu, ghi, L);
+          int pick = -1, lastpos = -1;
+          for (int e0 = e_lo; e0 < e_hi && pick < 0; e0 += 32) {
+            const int e = e0 + lane;
+            const float w = e < e_hi ? val(bufL[e]) : 0.f;
+            float ew = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const float y = __shfl_up_sync(0xffffffffu, ew, o);
+              if (lane >= o) ew += y;
+            }
+            const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
+            const unsigned pass = __ballot_sync(0xffffffffu, w > 0.f && __fadd_rn(run, ew) > d);
+            if (pass) pick = e0 + __ffs(pass) - 1;
+            if (pos) lastpos = e0 + 31 - __clz(pos);
+            run = __fadd_rn(run, __shfl_sync(0xffffffffu, ew, 31));
+          }
+          if (lane == 0 && (pick >= 0 || lastpos >= 0)) sh.claim = pick >= 0 ? pick : lastpos;
+        }
       }
-      if (found >= 0) atomicMin(&sh.claim, found);
       __syncthreads();
       if (sh.claim == INT_MAX) {  // take the last token of the slice with mass
         int lastpos = -1;
-        for (int i = lo; i < hi; ++i)
-          if (bufL[i] > 0.f) lastpos = i;
+        for (int i = tid; i < 4 * len4; i += STOCH_THREADS)
+          if (val(bufL[i]) > 0.f) lastpos = i;
         __syncthreads();
         if (tid == 0) sh.claim = -1;
         __syncthreads();
@@ -448,8 +536,7 @@ __global__ void __launch_bounds__(STOCH_THREADS, 1) k_verify_stoch(StochArgs a) 
     break;
   }
 
-  // write the path (CTA 0), then make sure no peer still reads this CTA's
-  // shared memory before it exits
+  // write the path (CTA 0); then no CTA exits while a peer may still send it a record
   if (rank == 0 && tid == 0) {
     const size_t row = (size_t)b * (a.max_depth + 1);
     const bool fits = depth <= a.max_depth;
@@ -467,16 +554,41 @@ __global__ void __launch_bounds__(STOCH_THREADS, 1) k_verify_stoch(StochArgs a) 
     const bool landed = mbar_wait(&sh.bar, phase ^ 1u, WAIT_NS);
     (void)landed;
   }
-  if (pending) cl_wait();
+  if (xcnt == 0) cl_wait();
   cl_arrive();
   cl_wait();
 }
 
 }  // namespace
 
-cudaError_t stoch_prepare() {
+// Opt-ins, once per device: the slices' shared memory and, where the GPU
+// allows it, clusters of 16 CTAs (otherwise clusters stay at 8).
+cudaError_t stoch_prepare(int* max_cluster) {
   const size_t smem = (size_t)2 * STOCH_MAX_SLICE * sizeof(float);
-  return cudaFuncSetAttribute(k_verify_stoch, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(k_verify_stoch, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  *max_cluster = STOCH_PORTABLE_CLUSTER;
+  if (cudaFuncSetAttribute(k_verify_stoch, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(STOCH_MAX_CLUSTER, 1);
+  cfg.blockDim = dim3(STOCH_THREADS);
+  cfg.dynamicSmemBytes = (size_t)2 * 8192 * sizeof(float);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = STOCH_MAX_CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_verify_stoch, &cfg) == cudaSuccess && n > 0)
+    *max_cluster = STOCH_MAX_CLUSTER;
+  else
+    (void)cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_verify_stoch(const StochArgs& a, cudaStream_t s) {
