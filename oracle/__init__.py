@@ -24,12 +24,13 @@ Modules:
   verify     — greedy argmax and the acceptance walk by definition.
   commit     — appending the accepted path's keys/values to the paged cache.
   stochastic — temperature verification by recursive rejection sampling.
+  dynamic    — reranking a draft's candidate pool into the tree to verify.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against
 the pages' worked example, closed forms, library routines on special cases, or
 brute force (see tests/test_oracle_*.py).  No function is "parity unpinned".
 """
-from . import tree, attention, verify, commit, stochastic  # noqa: F401
+from . import tree, attention, verify, commit, stochastic, dynamic  # noqa: F401
 
 # Status codes, restated here (the oracle shares no header with the library).
 OK = 0

@@ -447,6 +447,52 @@ def stochastic_workload(name: str, temperature: float = 1.0, batch: int = 64, ta
     return parent, stochastic_inputs(SEEDS[name], parent, VOCAB[name], temperature=temperature, tag=tag)
 
 
+# ----------------------------------------------------------------------------
+# candidate pools for dynamic tree construction
+# ----------------------------------------------------------------------------
+
+@dataclass
+class CandidatePool:
+    """What a draft hands over before reranking: an expanded candidate tree."""
+    parent: np.ndarray   # [B, M] int32, topological, parent[:, 0] = -1
+    logp: np.ndarray     # [B, M] fp32, the draft's log-probability of each candidate given its parent (root 0)
+    token: np.ndarray    # [B, M] int32, distinct among siblings
+
+
+def candidate_pool(seed: int, batch: int, depth: int, topk: int, vocab: int, tag: str = "pool") -> CandidatePool:
+    """A draft expansion of ``depth`` levels.  The root gets ``topk`` children;
+    on every later level the ``topk`` candidates of the previous level that the
+    draft gave the highest probability (given their own parent) get ``topk``
+    children each.  A parent's children
+    carry probabilities c * d, with d ~ Dirichlet(0.5, ..., 0.5) sorted in
+    descending order and c ~ U(0.5, 1) the mass the draft puts on its top-k,
+    and distinct uniform tokens.  Pool order is level by level."""
+    g = rng(seed, tag)
+    M = 1 + topk + (depth - 1) * topk * topk
+    parent = np.full((batch, M), -1, np.int32)
+    logp = np.zeros((batch, M), np.float32)
+    token = np.zeros((batch, M), np.int32)
+    for b in range(batch):
+        nxt = 1
+        level = [0]
+        for d in range(depth):
+            grow = level if d == 0 else sorted(sorted(level, key=lambda c: (-float(logp[b, c]), c))[:topk])
+            new_level = []
+            for u in grow:
+                probs = np.sort(g.dirichlet(np.full(topk, 0.5)))[::-1] * g.uniform(0.5, 1.0)
+                toks = g.choice(vocab, size=topk, replace=False)
+                for k in range(topk):
+                    parent[b, nxt] = u
+                    with np.errstate(divide="ignore"):
+                        logp[b, nxt] = np.float32(np.log(probs[k]))
+                    token[b, nxt] = toks[k]
+                    new_level.append(nxt)
+                    nxt += 1
+            level = new_level
+        assert nxt == M
+    return CandidatePool(parent=parent, logp=logp, token=token)
+
+
 # The five workloads.  Seeds: 20260000 + k unless overridden.
 
 def c1(seed: int = 20260001, **extra) -> Case:
