@@ -700,6 +700,111 @@ def run_stochastic(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_dynamic(args, world, rank, local):
+    """--part dynamic: time tree_build_dynamic (rerank a draft's candidate pool
+    into the N-node tree and build its masks, depths and positions) on pools
+    shaped for the workload's trees, beside tree_build_ancestry on the result."""
+    import torch
+    import workloads as W
+    import oracle
+    from tree_attention_speculative_gb300 import _build
+    _build.build()
+    import tree_attention_speculative_gb300 as ts
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    shapes = {"c1": (1, 2, 2, 5), "c2": (1, 6, 8, 64), "c4": (args.batch or 64, 8, 8, 64), "c5": (4, 10, 10, 192)}
+    if args.workload not in shapes:
+        raise SystemExit("--part dynamic takes c1, c2, c4 or c5")
+    B, depth, topk, N = shapes[args.workload]
+    pool = W.candidate_pool(W.SEEDS[args.workload], B, depth, topk, W.VOCAB[args.workload])
+    M = pool.parent.shape[1]
+    plen = np.full(B, 8192, np.int32)
+
+    def i32(x):
+        return torch.from_numpy(np.ascontiguousarray(x, np.int32)).to(dev)
+
+    pp, lp, tk, pl = i32(pool.parent), torch.from_numpy(pool.logp).to(dev), i32(pool.token), i32(plen)
+    Wd = (N + 63) // 64
+    out = dict(parent=torch.empty((B, N), dtype=torch.int32, device=dev),
+               tokens=torch.empty((B, N), dtype=torch.int32, device=dev),
+               sel=torch.empty((B, N), dtype=torch.int32, device=dev),
+               anc=torch.empty((B, N, Wd), dtype=torch.int64, device=dev),
+               depth=torch.empty((B, N), dtype=torch.int32, device=dev),
+               pos=torch.empty((B, N), dtype=torch.int32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+
+    def dyn():
+        ts.tree_build_dynamic(pp, lp, tk, pl, out["parent"], out["tokens"], out["sel"], out["anc"], out["depth"],
+                              out["pos"], out["status"])
+
+    def anc_only():
+        ts.tree_build_ancestry(out["parent"], pl, out["anc"], out["depth"], out["pos"], out["status"])
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        stream = torch.cuda.Stream(device=dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(steps):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    w0 = time.time()
+    ms = timed(dyn, args.steps)
+    w1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
+    assert (out["status"].cpu().numpy() == 0).all()
+    ms_anc = timed(anc_only, args.steps)
+    nbytes = B * M * 12 + B * N * (4 * 5 + 8 * Wd)   # pool in; tree, tokens, indices, depths, positions, masks out
+    pk = peaks()
+    cpu = None
+    if not args.no_cpu_baseline:
+        c0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - c0 < 3.0 or reps < 1:
+            oracle.dynamic.build_dynamic(pool.parent, pool.logp, pool.token, plen, N)
+            reps += 1
+        t_cpu = (time.perf_counter() - c0) / reps
+        cpu = {"value": B * N / t_cpu, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"the whole batch of this workload, {reps} repeats"}
+    line = {
+        "metric": "dynamic tree construction: tree tokens built/s", "value": B * N / (ms * 1e-3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}-shaped pools: B{B}, {depth} levels, top-{topk} expansion "
+                               f"(M={M} candidates) -> N={N}",
+                   "part": "dynamic", "ancestry_only_ms": ms_anc,
+                   "timing": "CUDA graph of the call alone, CUDA events; inputs stay in L2 (they are small)"},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "traffic": None,
+                     "kernel": "tree_build_dynamic", "algorithmic_bytes": nbytes,
+                     "note": "latency-bound: one CTA per sequence, a few KB each"},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: rank 0 alone, on the host cores."""
     if rank != 0:
@@ -752,17 +857,17 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch of c4 (smaller profiling case)")
     ap.add_argument("--prefix", type=int, default=0, help="override the prefix length of c5")
-    ap.add_argument("--part", choices=["step", "commit", "stochastic"], default="step",
+    ap.add_argument("--part", choices=["step", "commit", "stochastic", "dynamic"], default="step",
                     help="step: the verification step (default); commit: append accepted paths to the cache; "
-                         "stochastic: rejection-sampling verification")
+                         "stochastic: rejection-sampling verification; dynamic: tree construction from a pool")
     ap.add_argument("--temperature", type=float, default=1.0, help="sampling temperature of --part stochastic")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.steps <= 0:
         args.steps = default_steps(args.workload) if args.impl == "ours" else 3
-        if args.impl == "ours" and args.part == "stochastic":
-            args.steps = 3000   # about 0.25 s of timed work, long enough for the clock samples
+        if args.impl == "ours" and args.part in ("stochastic", "dynamic"):
+            args.steps = 3000   # a quarter of a second or more of timed work, long enough for the clock samples
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
@@ -770,6 +875,8 @@ def main(argv=None):
         run_commit(args, world, rank, local)
     elif args.part == "stochastic":
         run_stochastic(args, world, rank, local)
+    elif args.part == "dynamic":
+        run_dynamic(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

@@ -11,6 +11,11 @@
  *                        (paged KV cache) plus its own ancestors and itself
  *   tree_verify_greedy   greedy argmax of every node's logits and the
  *                        parent-chain acceptance walk
+ * and around it:
+ *   tree_build_dynamic      rerank a draft's candidate pool into the tree (and
+ *                           its masks) in place of tree_build_ancestry
+ *   tree_verify_stochastic  temperature verification by rejection sampling
+ *   tree_commit_accepted    append the accepted path to the paged cache
  *
  * Sources (web pages on the method):
  *   [P1] "Tree Attention", inferensys glossary.
@@ -30,8 +35,9 @@
  *   - Data-dependent errors (an invalid tree, a block id outside the pool, an
  *     internal wait that timed out) are written as a ts_status code into the
  *     caller's per-sequence int32 `status` array on the device.  A call never
- *     writes 0 there except tree_build_ancestry, which (re)initialises it, so
- *     one status array can be threaded through a whole step and read once.
+ *     writes 0 there except tree_build_ancestry and tree_build_dynamic, which
+ *     (re)initialise it, so one status array can be threaded through a whole
+ *     step and read once.
  *   - Index tensors are int32, row-major, densely packed.  bf16 tensors are
  *     16-bit brain-float, row-major, densely packed, 16-byte aligned.
  *   - Supported sizes: 1 <= N <= 256 nodes (W = ceil(N/64) <= 4 mask words),
@@ -300,6 +306,46 @@ TS_API ts_status tree_verify_stochastic(const int32_t* draft_tokens, const float
                                         const float* draft_probs, const int32_t* parent_idx, const float* coins,
                                         int B, int N, int V, int max_depth, float temperature, int32_t* accepted,
                                         int32_t* accept_len, int32_t* bonus, int32_t* status, ts_stream stream);
+
+/*
+ * tree_build_dynamic — choose the tree to verify from a draft's candidate
+ * pool, flatten it, and build its ancestry masks, depths and positions (the
+ * outputs of tree_build_ancestry) in one launch.
+ *
+ * [P2] Common Confusions: the tree shape may be selected dynamically; Where
+ * It Appears (EAGLE-2): the tree changes per context and the ancestry mask is
+ * built after reranking.  [P1] Key Mechanisms > Tree-Structured Candidate
+ * Generation.  The pages give no procedure; this call takes:
+ *   value(root) = 0, value(c) = value(parent(c)) + pool_logp[c], accumulated in
+ *   fp32 from the root down; the root and the N - 1 candidates of highest value
+ *   (ties: smaller pool index) are kept, in pool order.  With log-probabilities
+ *   <= 0 the kept set contains every kept node's parent.  Under the model in
+ *   which a draft token is accepted with the probability the draft gave it,
+ *   the kept tree maximises the expected number of accepted tokens over all
+ *   N-node trees cut from the pool.
+ *
+ *   pool_parent   [B, M] int32: topological (pool_parent[b,0] = -1 is the
+ *                 root, the last verified token; 0 <= pool_parent[b,c] < c).
+ *   pool_logp     [B, M] fp32: the draft's log-probability of each candidate
+ *                 given its parent, <= 0 (-inf allowed); the root's is unused.
+ *   pool_token    [B, M] int32: each candidate's token.
+ *   prefix_len    [B] int32: P_b, for the positions.
+ *   parent_idx    [B, N] int32 out: the kept tree, node k = k-th kept candidate.
+ *   draft_tokens  [B, N] int32 out: their tokens.
+ *   sel_index     [B, N] int32 out: their pool indices (to gather the draft's
+ *                 other per-candidate data).
+ *   anc_mask, depth, pos: out, as tree_build_ancestry for the kept tree.
+ *   status        [B] int32 out, (re)initialised like tree_build_ancestry:
+ *                 0, or TS_ERR_BAD_TREE for a pool that is not topological or
+ *                 has a positive or NaN log-probability (that sequence then
+ *                 gets a star tree: every node a child of the root).
+ * Returns TS_ERR_NULL / TS_ERR_SHAPE (B < 1, N < 1, M < N) /
+ * TS_ERR_UNSUPPORTED (N > 256, M > 1024) / TS_ERR_CUDA.
+ */
+TS_API ts_status tree_build_dynamic(const int32_t* pool_parent, const float* pool_logp, const int32_t* pool_token,
+                                    const int32_t* prefix_len, int B, int M, int N, int32_t* parent_idx,
+                                    int32_t* draft_tokens, int32_t* sel_index, uint64_t* anc_mask, int32_t* depth,
+                                    int32_t* pos, int32_t* status, ts_stream stream);
 
 /* Size of the library-owned scratch behind tree_verify_greedy_noalloc. */
 #define TS_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)

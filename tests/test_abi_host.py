@@ -136,3 +136,36 @@ def test_verify_and_ancestry_reject_before_launch(ts):
     assert L.tree_verify_greedy(*bad) == -4
     bad = list(args); bad[13] = need - 1
     assert L.tree_verify_greedy(*bad) == -8
+
+
+def test_commit_stochastic_and_dynamic_reject_before_launch(ts):
+    L = ts.lib()
+    a = ctypes.c_void_p(0x10000)
+    # tree_commit_accepted: k_tree, v_tree, accepted, accept_len, prefix_len, k_cache, v_cache, table,
+    #                       B, N, Hkv, D, bs, num_blocks, max_blocks, max_depth, new_len, status, stream
+    args = [a, a, a, a, a, a, a, a, 2, 8, 2, 128, 16, 10, 4, 4, a, a, None]
+    bad = list(args); bad[0] = None
+    assert L.tree_commit_accepted(*bad) == -1
+    bad = list(args); bad[11] = 96
+    assert L.tree_commit_accepted(*bad) == -4
+    bad = list(args); bad[8] = 0
+    assert L.tree_commit_accepted(*bad) == -2
+    # tree_verify_stochastic: draft, logits, q, parent, coins, B, N, V, max_depth, T, acc, L, bonus, status, stream
+    args = [a, a, a, a, a, 4, 64, 128256, 8, ctypes.c_float(1.0), a, a, a, a, None]
+    bad = list(args); bad[2] = None
+    assert L.tree_verify_stochastic(*bad) == -1
+    for i, v in ((9, ctypes.c_float(0.0)), (9, ctypes.c_float(-1.0)), (9, ctypes.c_float(float("inf"))),
+                 (6, 257), (7, 409601), (8, -1), (5, 70000)):
+        bad = list(args); bad[i] = v
+        assert L.tree_verify_stochastic(*bad) == -4, (i, v)
+    # tree_build_dynamic: pool_parent, logp, token, prefix_len, B, M, N, parent, tokens, sel, anc, depth, pos,
+    #                     status, stream
+    args = [a, a, a, a, 4, 457, 64, a, a, a, a, a, a, a, None]
+    bad = list(args); bad[1] = None
+    assert L.tree_build_dynamic(*bad) == -1
+    bad = list(args); bad[5] = 63
+    assert L.tree_build_dynamic(*bad) == -2
+    bad = list(args); bad[5] = 1025
+    assert L.tree_build_dynamic(*bad) == -4
+    bad = list(args); bad[6] = 257; bad[5] = 1000
+    assert L.tree_build_dynamic(*bad) == -4

@@ -21,7 +21,8 @@ from ._build import LIB as LIB_PATH
 __all__ = [
     "TreeSpecError", "lib", "ts_status_str", "tree_build_ancestry", "AttnParams", "attn_params",
     "tree_attn_workspace_size", "tree_attn_fwd", "tree_verify_workspace_size", "tree_verify_greedy",
-    "tree_verify_greedy_noalloc", "tree_commit_accepted", "tree_verify_stochastic", "NOALLOC_SCRATCH_BYTES",
+    "tree_verify_greedy_noalloc", "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic",
+    "NOALLOC_SCRATCH_BYTES",
     "STATUS",
 ]
 
@@ -55,7 +56,7 @@ _LIB: Optional[ctypes.CDLL] = None
 # every symbol include/treespec.h declares
 EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_fwd",
            "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc",
-           "tree_commit_accepted", "tree_verify_stochastic")
+           "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic")
 
 # TS_VERIFY_NOALLOC_SCRATCH_BYTES of treespec.h
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -89,6 +90,8 @@ def lib() -> ctypes.CDLL:
         L.tree_verify_stochastic.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp,
                                              vp]
         L.tree_verify_stochastic.restype = i32
+        L.tree_build_dynamic.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.tree_build_dynamic.restype = i32
         _LIB = L
     return _LIB
 
@@ -185,6 +188,17 @@ def tree_verify_stochastic(draft_tokens, target_logits, draft_probs, parent_idx,
                                         _p(coins), B, N, V, accepted.shape[1] - 1, float(temperature),
                                         _p(accepted), _p(accept_len), _p(bonus), _p(status), _s(stream)),
            "tree_verify_stochastic")
+
+
+def tree_build_dynamic(pool_parent, pool_logp, pool_token, prefix_len, parent_idx, draft_tokens, sel_index,
+                       anc_mask, depth, pos, status, stream=None) -> None:
+    """Rerank a candidate pool [B, M] into the N-node tree of parent_idx [B, N]
+    and build its masks, depths and positions."""
+    B, M = pool_parent.shape
+    N = parent_idx.shape[1]
+    _check(lib().tree_build_dynamic(_p(pool_parent), _p(pool_logp), _p(pool_token), _p(prefix_len), B, M, N,
+                                    _p(parent_idx), _p(draft_tokens), _p(sel_index), _p(anc_mask), _p(depth),
+                                    _p(pos), _p(status), _s(stream)), "tree_build_dynamic")
 
 
 def tree_verify_greedy_noalloc(draft_tokens, target_logits, parent_idx, max_depth: int, accepted, accept_len, bonus,

@@ -308,6 +308,26 @@ ts_status tree_verify_stochastic(const int32_t* draft_tokens, const float* targe
   return launch_verify_stoch(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
+ts_status tree_build_dynamic(const int32_t* pool_parent, const float* pool_logp, const int32_t* pool_token,
+                             const int32_t* prefix_len, int B, int M, int N, int32_t* parent_idx,
+                             int32_t* draft_tokens, int32_t* sel_index, uint64_t* anc_mask, int32_t* depth,
+                             int32_t* pos, int32_t* status, ts_stream stream) {
+  if (!pool_parent || !pool_logp || !pool_token || !prefix_len || !parent_idx || !draft_tokens || !sel_index ||
+      !anc_mask || !depth || !pos || !status)
+    return TS_ERR_NULL;
+  if (B < 1 || N < 1 || M < N) return TS_ERR_SHAPE;
+  if (N > MAX_NODES || M > DYN_MAX_POOL) return TS_ERR_UNSUPPORTED;
+  DynArgs a{};
+  a.pool_parent = pool_parent;
+  a.pool_logp = pool_logp;
+  a.pool_token = pool_token;
+  a.prefix_len = prefix_len;
+  a.B = B; a.M = M; a.N = N;
+  a.parent_idx = parent_idx; a.draft_tokens = draft_tokens; a.sel_index = sel_index; a.anc_mask = anc_mask;
+  a.depth = depth; a.pos = pos; a.status = status;
+  return launch_build_dynamic(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
 ts_status tree_verify_greedy_noalloc(const int32_t* draft_tokens, const float* target_logits,
                                      const int32_t* parent_idx, int B, int N, int V, int max_depth,
                                      int32_t* accepted, int32_t* accept_len, int32_t* bonus,

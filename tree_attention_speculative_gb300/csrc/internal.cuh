@@ -168,6 +168,24 @@ constexpr int STOCH_PORTABLE_CLUSTER = 8;
 constexpr int STOCH_TARGET_SLICE = 8192;               // the cluster grows until a slice is this small
 constexpr int STOCH_MAX_SLICE = 25600;                 // 2 x 100 KB of shared memory per CTA
 cudaError_t stoch_prepare(int* max_cluster);
+
+// Dynamic tree construction: one CTA per sequence over a candidate pool.
+struct DynArgs {
+  const int32_t* pool_parent;
+  const float* pool_logp;
+  const int32_t* pool_token;
+  const int32_t* prefix_len;
+  int B, M, N;
+  int32_t* parent_idx;
+  int32_t* draft_tokens;
+  int32_t* sel_index;
+  uint64_t* anc_mask;
+  int32_t* depth;
+  int32_t* pos;
+  int32_t* status;
+};
+constexpr int DYN_MAX_POOL = 1024;
+cudaError_t launch_build_dynamic(const DynArgs& a, cudaStream_t s);
 cudaError_t launch_verify_stoch(const StochArgs& a, cudaStream_t s);
 
 }  // namespace ts
