@@ -16,7 +16,8 @@ Sources (three web pages on the method):
        Tradeoffs, Common Confusions).
   [P3] "Speculative Tree Attention: How Multi-Candidate Draft Models and Parallel
        Verification Deliver 4x LLM Speedups" — premlal news (code listing:
-       TreeNode, build_tree_attention_mask, verify_candidate_tree, demo).
+       TreeNode, build_tree_attention_mask, verify_candidate_tree, demo;
+       sections Production Inference Runtimes, The Future of Reasoning).
 
 Modules:
   tree       — tree validity, ancestry mask by parent walk, depth, positions.
@@ -25,12 +26,13 @@ Modules:
   commit     — appending the accepted path's keys/values to the paged cache.
   stochastic — temperature verification by recursive rejection sampling.
   dynamic    — reranking a draft's candidate pool into the tree to verify.
+  forest     — several roots in one flattened sequence: masks and acceptance.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against
 the pages' worked example, closed forms, library routines on special cases, or
 brute force (see tests/test_oracle_*.py).  No function is "parity unpinned".
 """
-from . import tree, attention, verify, commit, stochastic, dynamic  # noqa: F401
+from . import tree, attention, verify, commit, stochastic, dynamic, forest  # noqa: F401
 
 # Status codes, restated here (the oracle shares no header with the library).
 OK = 0

@@ -156,6 +156,27 @@ def tree_star(n: int) -> np.ndarray:
     return p
 
 
+def forest_random(g: np.random.Generator, n: int, roots: int, max_depth: int) -> np.ndarray:
+    """A forest of ``roots`` random trees (``tree_random_levels``) with ``n`` nodes in
+    all, flattened level by level with the trees interleaved (node 0 is a root)."""
+    sizes = np.full(roots, n // roots)
+    sizes[: n % roots] += 1
+    comps = [tree_random_levels(g, int(k), min(max_depth, int(k) - 1)) if k > 1 else np.array([-1], np.int32)
+             for k in sizes]
+    nodes = []  # (level, tiebreak, component, local index)
+    for ci, par in enumerate(comps):
+        lv = _levels_of(par)
+        for j in range(len(par)):
+            nodes.append((int(lv[j]), float(g.random()), ci, j))
+    nodes.sort()
+    where = {(ci, j): k for k, (_, _, ci, j) in enumerate(nodes)}
+    out = np.full(n, -1, np.int32)
+    for k, (_, _, ci, j) in enumerate(nodes):
+        p = int(comps[ci][j])
+        out[k] = -1 if p < 0 else where[(ci, p)]
+    return out
+
+
 def tree_random_recursive(g: np.random.Generator, n: int) -> np.ndarray:
     """parent[i] uniform over [0, i): a random recursive tree (deep-ish, irregular)."""
     p = np.full(n, -1, np.int32)
