@@ -210,7 +210,8 @@ def oracle_sample_step(case):
     units_total = case.B * case.Hkv
     rows_total = case.B * case.N
     t0 = time.perf_counter()
-    oracle.tree.build_ancestry(case.parent, case.prefix_len)
+    forest = bool((case.parent[:, 1:] < 0).any())
+    (oracle.forest.build_ancestry_forest if forest else oracle.tree.build_ancestry)(case.parent, case.prefix_len)
     t1 = time.perf_counter()
     oracle.attention.tree_attention_case(case, units=[(0, 0)])
     t2 = time.perf_counter()
@@ -221,7 +222,8 @@ def oracle_sample_step(case):
         lg = case.logits.reshape(rows_total, case.vocab)[:vrows]
         oracle.verify.greedy_argmax(lg)
         am = oracle.verify.greedy_argmax(case.logits[0])
-        oracle.verify.accept_walk(case.parent[0], case.draft[0], am, case.N)
+        (oracle.forest.accept_walk_forest if forest else oracle.verify.accept_walk)(case.parent[0], case.draft[0], am,
+                                                                                    case.N)
         t_ver = time.perf_counter() - t2
     full = (t1 - t0) + (t2 - t1) * units_total + (t_ver * rows_total / max(vrows, 1) if vrows else 0.0)
     desc = (f"ancestry of all {case.B} trees; attention of 1 of {units_total} (sequence, kv-head) units x "
@@ -282,7 +284,7 @@ def run_ours(args, world, rank, local):
     dsets = [to_dev(c, dev) for c in cases]
     # one set of output buffers per input set (prefix lengths, hence the split plan, may differ)
     steps = [TreeVerifyStep(c.B, c.N, c.Hq, c.Hkv, c.D, c.prefix_len, vocab=c.vocab, max_depth=c.N - 1,
-                            device=dev) for c in cases]
+                            device=dev, forest=bool(args.forest)) for c in cases]
     step = steps[0]
 
     def enqueue(k, evs=None):
@@ -476,7 +478,9 @@ def run_ours(args, world, rank, local):
         "value": value, "unit": "tree tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: " + WORKLOAD_DESC[args.workload], "batch": base.B,
+        "config": {"workload": f"{args.workload}: " + WORKLOAD_DESC[args.workload] +
+                               (f"; each tree replaced by a forest of {args.forest} trees" if args.forest else ""),
+                   "batch": base.B,
                    "tree_nodes": base.N, "q_heads": base.Hq, "kv_heads": base.Hkv, "head_dim": base.D,
                    "prefix": [int(x) for x in np.unique(base.prefix_len)][:4], "kv_block": base.bs,
                    "vocab": base.vocab, "parallelism": f"replicas x{world}",
@@ -839,6 +843,10 @@ def workload_overrides(args) -> dict:
         if args.workload != "c5":
             raise SystemExit("--prefix applies to c5 only")
         kw["prefix"] = args.prefix
+    if getattr(args, "forest", 0):
+        if args.workload not in ("c2", "c4", "c5"):
+            raise SystemExit("--forest applies to c2, c4 and c5")
+        kw["forest_roots"] = args.forest
     return kw
 
 
@@ -861,6 +869,8 @@ def main(argv=None):
                     help="step: the verification step (default); commit: append accepted paths to the cache; "
                          "stochastic: rejection-sampling verification; dynamic: tree construction from a pool")
     ap.add_argument("--temperature", type=float, default=1.0, help="sampling temperature of --part stochastic")
+    ap.add_argument("--forest", type=int, default=0,
+                    help="replace each sequence's tree by a forest of this many trees (same nodes and depth)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

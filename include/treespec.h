@@ -14,6 +14,8 @@
  * and around it:
  *   tree_build_dynamic      rerank a draft's candidate pool into the tree (and
  *                           its masks) in place of tree_build_ancestry
+ *   tree_build_ancestry_forest, tree_verify_greedy_forest
+ *                           the same for several roots per sequence
  *   tree_verify_stochastic  temperature verification by rejection sampling
  *   tree_commit_accepted    append the accepted path to the paged cache
  *
@@ -35,8 +37,8 @@
  *   - Data-dependent errors (an invalid tree, a block id outside the pool, an
  *     internal wait that timed out) are written as a ts_status code into the
  *     caller's per-sequence int32 `status` array on the device.  A call never
- *     writes 0 there except tree_build_ancestry and tree_build_dynamic, which
- *     (re)initialise it, so one status array can be threaded through a whole
+ *     writes 0 there except tree_build_ancestry(_forest) and tree_build_dynamic,
+ *     which (re)initialise it, so one status array can be threaded through a whole
  *     step and read once.
  *   - Index tensors are int32, row-major, densely packed.  bf16 tensors are
  *     16-bit brain-float, row-major, densely packed, 16-byte aligned.
@@ -346,6 +348,35 @@ TS_API ts_status tree_build_dynamic(const int32_t* pool_parent, const float* poo
                                     const int32_t* prefix_len, int B, int M, int N, int32_t* parent_idx,
                                     int32_t* draft_tokens, int32_t* sel_index, uint64_t* anc_mask, int32_t* depth,
                                     int32_t* pos, int32_t* status, ts_stream stream);
+
+/*
+ * Forests: several draft trees in one flattened sequence.
+ *
+ * [P3] The Future of Reasoning: the verifier evaluates whole forests of
+ * candidate continuations in parallel.  The pages give no rule; the tree rules
+ * carry over as follows.  Node 0 is a root (parent -1); any later node may be
+ * another root (parent -1) or have a parent with a smaller index.  Every root
+ * is a given token attended at position P_b, like a tree's root.  A node's
+ * mask, depth and position follow its chain to its own root, so nodes of
+ * different trees never see each other; tree_attn_fwd and
+ * tree_commit_accepted need nothing new.  Acceptance: every root is accepted;
+ * node c is accepted iff every node x on its chain below its root has
+ * draft[x] == argmax(logits[parent(x)]); n* is the deepest accepted node of the
+ * forest (ties: smallest index); the accepted row runs from n*'s root to n*.
+ *
+ * tree_build_ancestry_forest and tree_verify_greedy_forest take exactly the
+ * arguments of tree_build_ancestry and tree_verify_greedy (same workspace
+ * size) and report the same status codes; only the validity rule and the
+ * root of a chain differ.
+ */
+TS_API ts_status tree_build_ancestry_forest(const int32_t* parent_idx, const int32_t* prefix_len, int B, int N,
+                                            uint64_t* anc_mask, int32_t* depth, int32_t* pos, int32_t* status,
+                                            ts_stream stream);
+TS_API ts_status tree_verify_greedy_forest(const int32_t* draft_tokens, const float* target_logits,
+                                           const int32_t* parent_idx, int B, int N, int V, int max_depth,
+                                           int32_t* accepted, int32_t* accept_len, int32_t* bonus,
+                                           int32_t* argmax_out, int32_t* status, void* workspace,
+                                           size_t workspace_bytes, ts_stream stream);
 
 /* Size of the library-owned scratch behind tree_verify_greedy_noalloc. */
 #define TS_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)

@@ -169,3 +169,16 @@ def test_commit_stochastic_and_dynamic_reject_before_launch(ts):
     assert L.tree_build_dynamic(*bad) == -4
     bad = list(args); bad[6] = 257; bad[5] = 1000
     assert L.tree_build_dynamic(*bad) == -4
+
+
+def test_forest_calls_reject_before_launch(ts):
+    L = ts.lib()
+    a = ctypes.c_void_p(0x10000)
+    assert L.tree_build_ancestry_forest(None, a, 1, 5, a, a, a, a, None) == -1
+    assert L.tree_build_ancestry_forest(a, a, 1, 257, a, a, a, a, None) == -4
+    need = ts.tree_verify_workspace_size(4, 64, 128256)
+    args = [a, a, a, 4, 64, 128256, 8, a, a, a, a, a, a, need, None]
+    bad = list(args); bad[2] = None
+    assert L.tree_verify_greedy_forest(*bad) == -1
+    bad = list(args); bad[13] = need - 1
+    assert L.tree_verify_greedy_forest(*bad) == -8

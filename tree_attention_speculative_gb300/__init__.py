@@ -22,7 +22,7 @@ __all__ = [
     "TreeSpecError", "lib", "ts_status_str", "tree_build_ancestry", "AttnParams", "attn_params",
     "tree_attn_workspace_size", "tree_attn_fwd", "tree_verify_workspace_size", "tree_verify_greedy",
     "tree_verify_greedy_noalloc", "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic",
-    "NOALLOC_SCRATCH_BYTES",
+    "tree_build_ancestry_forest", "tree_verify_greedy_forest", "NOALLOC_SCRATCH_BYTES",
     "STATUS",
 ]
 
@@ -56,7 +56,8 @@ _LIB: Optional[ctypes.CDLL] = None
 # every symbol include/treespec.h declares
 EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_fwd",
            "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc",
-           "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic")
+           "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic", "tree_build_ancestry_forest",
+           "tree_verify_greedy_forest")
 
 # TS_VERIFY_NOALLOC_SCRATCH_BYTES of treespec.h
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -92,6 +93,10 @@ def lib() -> ctypes.CDLL:
         L.tree_verify_stochastic.restype = i32
         L.tree_build_dynamic.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.tree_build_dynamic.restype = i32
+        L.tree_build_ancestry_forest.argtypes = L.tree_build_ancestry.argtypes
+        L.tree_build_ancestry_forest.restype = i32
+        L.tree_verify_greedy_forest.argtypes = L.tree_verify_greedy.argtypes
+        L.tree_verify_greedy_forest.restype = i32
         _LIB = L
     return _LIB
 
@@ -121,6 +126,14 @@ def tree_build_ancestry(parent_idx: torch.Tensor, prefix_len: torch.Tensor, anc_
     B, N = parent_idx.shape
     _check(lib().tree_build_ancestry(_p(parent_idx), _p(prefix_len), B, N, _p(anc_mask), _p(depth), _p(pos),
                                      _p(status), _s(stream)), "tree_build_ancestry")
+
+
+def tree_build_ancestry_forest(parent_idx: torch.Tensor, prefix_len: torch.Tensor, anc_mask: torch.Tensor,
+                               depth: torch.Tensor, pos: torch.Tensor, status: torch.Tensor, stream=None) -> None:
+    """tree_build_ancestry for forests (several parent -1 entries; node 0 is a root)."""
+    B, N = parent_idx.shape
+    _check(lib().tree_build_ancestry_forest(_p(parent_idx), _p(prefix_len), B, N, _p(anc_mask), _p(depth), _p(pos),
+                                            _p(status), _s(stream)), "tree_build_ancestry_forest")
 
 
 def attn_params(q, k_cache, v_cache, block_table, prefix_len, prefix_len_host, k_tree, v_tree, anc_mask, pos,
@@ -166,6 +179,16 @@ def tree_verify_greedy(draft_tokens, target_logits, parent_idx, max_depth: int, 
                                     _p(accepted), _p(accept_len), _p(bonus), _p(argmax_out), _p(status),
                                     _p(workspace), workspace.numel() * workspace.element_size(), _s(stream)),
            "tree_verify_greedy")
+
+
+def tree_verify_greedy_forest(draft_tokens, target_logits, parent_idx, max_depth: int, accepted, accept_len, bonus,
+                              argmax_out, status, workspace, stream=None) -> None:
+    """tree_verify_greedy for forests; same workspace size."""
+    B, N, V = target_logits.shape
+    _check(lib().tree_verify_greedy_forest(_p(draft_tokens), _p(target_logits), _p(parent_idx), B, N, V, max_depth,
+                                           _p(accepted), _p(accept_len), _p(bonus), _p(argmax_out), _p(status),
+                                           _p(workspace), workspace.numel() * workspace.element_size(), _s(stream)),
+           "tree_verify_greedy_forest")
 
 
 def tree_commit_accepted(k_tree, v_tree, accepted, accept_len, prefix_len, k_cache, v_cache, block_table,

@@ -4,6 +4,10 @@
 // Tradeoffs ("position bookkeeping"); [P3] code listing,
 // build_tree_attention_mask (walk parent pointers to the root).
 //
+// A forest (several roots, [P3] The Future of Reasoning) differs only in the
+// validity rule: any node may have parent -1; every chain then stops at its
+// own root.
+//
 // One CTA per sequence, one thread per node.  Parents are staged in shared
 // memory; each thread validates its own parent pointer, the CTA agrees on the
 // tree's validity with one barrier-and, then each node walks its chain to the
@@ -16,7 +20,7 @@ namespace ts {
 __global__ void __launch_bounds__(MAX_NODES)
 k_ancestry(const int32_t* __restrict__ parent, const int32_t* __restrict__ prefix_len, int N, int W,
            uint64_t* __restrict__ anc, int32_t* __restrict__ depth, int32_t* __restrict__ pos,
-           int32_t* __restrict__ status) {
+           int32_t* __restrict__ status, int forest) {
   __shared__ int sp[MAX_NODES];
   const int b = blockIdx.x;
   const int i = threadIdx.x;
@@ -26,7 +30,8 @@ k_ancestry(const int32_t* __restrict__ parent, const int32_t* __restrict__ prefi
   bool ok = true;
   if (i < N) {
     p = parent[(size_t)b * N + i];
-    ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
+    // a forest may start a new tree (parent -1) at any node; node 0 is always a root
+    ok = (i == 0) ? (p == -1) : ((p >= 0 && p < i) || (forest && p == -1));
     sp[i] = p;
   }
   const int valid = __syncthreads_and(ok);
@@ -61,10 +66,10 @@ k_ancestry(const int32_t* __restrict__ parent, const int32_t* __restrict__ prefi
 
 cudaError_t launch_ancestry(const int32_t* parent, const int32_t* prefix_len, int B, int N,
                             uint64_t* anc, int32_t* depth, int32_t* pos, int32_t* status,
-                            cudaStream_t s) {
+                            cudaStream_t s, int forest) {
   const int threads = ceil_div(N, 32) * 32;
   return launch_pdl(k_ancestry, dim3(B), dim3(threads), 0, s, parent, prefix_len, N, ceil_div(N, 64), anc, depth,
-                    pos, status);
+                    pos, status, forest);
 }
 
 }  // namespace ts

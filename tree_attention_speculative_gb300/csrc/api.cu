@@ -139,6 +139,33 @@ VerifyPlan plan_verify(int B, int N, int V) {
   return pl;
 }
 
+ts_status verify_greedy_impl(const int32_t* draft_tokens, const float* target_logits, const int32_t* parent_idx,
+                             int B, int N, int V, int max_depth, int32_t* accepted, int32_t* accept_len,
+                             int32_t* bonus, int32_t* argmax_out, int32_t* status, void* workspace,
+                             size_t workspace_bytes, ts_stream stream, int forest) {
+  if (!draft_tokens || !target_logits || !parent_idx || !accepted || !accept_len || !bonus ||
+      !argmax_out || !status)
+    return TS_ERR_NULL;
+  if (B < 1 || N < 1 || N > MAX_NODES || V < 1 || max_depth < 0) return TS_ERR_UNSUPPORTED;
+  const VerifyPlan pl = plan_verify(B, N, V);
+  if (!workspace || workspace_bytes < pl.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return TS_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  VerifyArgs a{};
+  a.draft = draft_tokens;
+  a.logits = target_logits;
+  a.parent = parent_idx;
+  a.B = B; a.N = N; a.V = V; a.max_depth = max_depth; a.chunks = pl.chunks;
+  a.accepted = accepted; a.accept_len = accept_len; a.bonus = bonus; a.argmax = argmax_out;
+  a.status = status;
+  a.row_ticket = reinterpret_cast<unsigned*>(ws + pl.row_ticket);
+  a.seq_ticket = reinterpret_cast<unsigned*>(ws + pl.seq_ticket);
+  a.part_v = reinterpret_cast<float*>(ws + pl.part_v);
+  a.part_i = reinterpret_cast<int32_t*>(ws + pl.part_i);
+  a.forest = forest;
+  return launch_verify(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace ts
 
@@ -168,6 +195,16 @@ ts_status tree_build_ancestry(const int32_t* parent_idx, const int32_t* prefix_l
   if (B < 1 || N < 1 || N > MAX_NODES) return TS_ERR_UNSUPPORTED;
   cudaError_t e = launch_ancestry(parent_idx, prefix_len, B, N, anc_mask, depth, pos, status,
                                   (cudaStream_t)stream);
+  return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+ts_status tree_build_ancestry_forest(const int32_t* parent_idx, const int32_t* prefix_len, int B, int N,
+                                     uint64_t* anc_mask, int32_t* depth, int32_t* pos, int32_t* status,
+                                     ts_stream stream) {
+  if (!parent_idx || !prefix_len || !anc_mask || !depth || !pos || !status) return TS_ERR_NULL;
+  if (B < 1 || N < 1 || N > MAX_NODES) return TS_ERR_UNSUPPORTED;
+  cudaError_t e = launch_ancestry(parent_idx, prefix_len, B, N, anc_mask, depth, pos, status,
+                                  (cudaStream_t)stream, 1);
   return e == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
@@ -224,26 +261,17 @@ ts_status tree_verify_greedy(const int32_t* draft_tokens, const float* target_lo
                              int32_t* accepted, int32_t* accept_len, int32_t* bonus,
                              int32_t* argmax_out, int32_t* status, void* workspace,
                              size_t workspace_bytes, ts_stream stream) {
-  if (!draft_tokens || !target_logits || !parent_idx || !accepted || !accept_len || !bonus ||
-      !argmax_out || !status)
-    return TS_ERR_NULL;
-  if (B < 1 || N < 1 || N > MAX_NODES || V < 1 || max_depth < 0) return TS_ERR_UNSUPPORTED;
-  const VerifyPlan pl = plan_verify(B, N, V);
-  if (!workspace || workspace_bytes < pl.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
-    return TS_ERR_WORKSPACE;
-  char* ws = static_cast<char*>(workspace);
-  VerifyArgs a{};
-  a.draft = draft_tokens;
-  a.logits = target_logits;
-  a.parent = parent_idx;
-  a.B = B; a.N = N; a.V = V; a.max_depth = max_depth; a.chunks = pl.chunks;
-  a.accepted = accepted; a.accept_len = accept_len; a.bonus = bonus; a.argmax = argmax_out;
-  a.status = status;
-  a.row_ticket = reinterpret_cast<unsigned*>(ws + pl.row_ticket);
-  a.seq_ticket = reinterpret_cast<unsigned*>(ws + pl.seq_ticket);
-  a.part_v = reinterpret_cast<float*>(ws + pl.part_v);
-  a.part_i = reinterpret_cast<int32_t*>(ws + pl.part_i);
-  return launch_verify(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+  return ts::verify_greedy_impl(draft_tokens, target_logits, parent_idx, B, N, V, max_depth, accepted, accept_len,
+                                bonus, argmax_out, status, workspace, workspace_bytes, stream, 0);
+}
+
+ts_status tree_verify_greedy_forest(const int32_t* draft_tokens, const float* target_logits,
+                                    const int32_t* parent_idx, int B, int N, int V, int max_depth,
+                                    int32_t* accepted, int32_t* accept_len, int32_t* bonus,
+                                    int32_t* argmax_out, int32_t* status, void* workspace,
+                                    size_t workspace_bytes, ts_stream stream) {
+  return ts::verify_greedy_impl(draft_tokens, target_logits, parent_idx, B, N, V, max_depth, accepted, accept_len,
+                                bonus, argmax_out, status, workspace, workspace_bytes, stream, 1);
 }
 
 ts_status tree_commit_accepted(const void* k_tree, const void* v_tree, const int32_t* accepted,

@@ -105,7 +105,7 @@ struct AttnPlan {
 
 cudaError_t launch_ancestry(const int32_t* parent, const int32_t* prefix_len, int B, int N,
                             uint64_t* anc, int32_t* depth, int32_t* pos, int32_t* status,
-                            cudaStream_t s);
+                            cudaStream_t s, int forest = 0);
 cudaError_t attn_tc_prepare();
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s);
@@ -124,6 +124,7 @@ struct VerifyArgs {
   int32_t* part_i;
   unsigned* row_ticket;
   unsigned* seq_ticket;
+  int forest;  // several roots allowed; chains stop at -1
 };
 constexpr int VERIFY_THREADS = 256;
 constexpr int VERIFY_CHUNK = 8192;  // logits per CTA

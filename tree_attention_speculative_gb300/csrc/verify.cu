@@ -146,7 +146,7 @@ k_verify(VerifyArgs a) {
   bool ok = true;
   if (t < N) {
     const int p = a.parent[(size_t)b * N + t];
-    ok = (t == 0) ? (p == -1) : (p >= 0 && p < t);
+    ok = (t == 0) ? (p == -1) : ((p >= 0 && p < t) || (a.forest && p == -1));
     s_par[t] = p;
     s_draft[t] = a.draft[(size_t)b * N + t];
     s_pred[t] = __ldcg(a.argmax + (size_t)b * N + t);
@@ -163,13 +163,14 @@ k_verify(VerifyArgs a) {
     return;
   }
   // key = (depth << 16) | (0xFFFF - node) for accepted nodes: the maximum key
-  // is the deepest accepted node, smallest index on ties.  The root is always
-  // accepted, so the maximum is never the -1 of a rejected node.
+  // is the deepest accepted node, smallest index on ties.  The root (every
+  // root of a forest) is always accepted, so the maximum is never the -1 of a
+  // rejected node.  A chain ends at its root, the node whose parent is -1.
   int key = -1;
   if (t < N) {
     bool acc = true;
     int d = 0, y = t;
-    while (y != 0) {
+    while (s_par[y] != -1) {
       const int p = s_par[y];
       acc = acc && (s_draft[y] == s_pred[p]);
       y = p;

@@ -2,8 +2,9 @@
 
 ``TreeVerifyStep`` owns the output and workspace buffers (allocated with torch,
 which is only the allocator here) for fixed sizes and enqueues
-tree_build_ancestry -> tree_attn_fwd -> tree_verify_greedy on one stream.  Every
-computation happens in the library's kernels.
+tree_build_ancestry -> tree_attn_fwd -> tree_verify_greedy on one stream (their
+_forest variants with ``forest=True``).  Every computation happens in the
+library's kernels.
 """
 from __future__ import annotations
 
@@ -13,13 +14,15 @@ import numpy as np
 import torch
 
 from . import (attn_params, tree_attn_fwd, tree_attn_workspace_size, tree_build_ancestry,
-               tree_verify_greedy, tree_verify_workspace_size)
+               tree_build_ancestry_forest, tree_verify_greedy, tree_verify_greedy_forest,
+               tree_verify_workspace_size)
 
 
 class TreeVerifyStep:
     def __init__(self, B: int, N: int, Hq: int, Hkv: int, D: int, prefix_len_host, vocab: int = 0,
-                 max_depth: Optional[int] = None, device="cuda", scale: float = 0.0):
+                 max_depth: Optional[int] = None, device="cuda", scale: float = 0.0, forest: bool = False):
         self.B, self.N, self.Hq, self.Hkv, self.D = B, N, Hq, Hkv, D
+        self.forest = forest
         self.vocab = vocab
         self.max_depth = N - 1 if max_depth is None else max_depth
         self.scale = scale
@@ -52,7 +55,8 @@ class TreeVerifyStep:
         return tree_attn_workspace_size(self._params(q, k_cache, v_cache, block_table, prefix_len, k_tree, v_tree))
 
     def ancestry(self, parent, prefix_len, stream=None):
-        tree_build_ancestry(parent, prefix_len, self.anc, self.depth, self.pos, self.status, stream)
+        build = tree_build_ancestry_forest if self.forest else tree_build_ancestry
+        build(parent, prefix_len, self.anc, self.depth, self.pos, self.status, stream)
 
     def attention(self, q, k_cache, v_cache, block_table, prefix_len, k_tree, v_tree, stream=None):
         p = self._params(q, k_cache, v_cache, block_table, prefix_len, k_tree, v_tree)
@@ -64,8 +68,9 @@ class TreeVerifyStep:
         tree_attn_fwd(p, self.ws_attn, stream)
 
     def verify(self, draft, logits, parent, stream=None):
-        tree_verify_greedy(draft, logits, parent, self.max_depth, self.accepted, self.accept_len, self.bonus,
-                           self.argmax, self.status, self.ws_verify, stream)
+        verify = tree_verify_greedy_forest if self.forest else tree_verify_greedy
+        verify(draft, logits, parent, self.max_depth, self.accepted, self.accept_len, self.bonus, self.argmax,
+               self.status, self.ws_verify, stream)
 
     def run(self, parent, prefix_len, q, k_cache, v_cache, block_table, k_tree, v_tree, draft=None, logits=None,
             stream=None):

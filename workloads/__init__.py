@@ -186,17 +186,19 @@ def tree_random_recursive(g: np.random.Generator, n: int) -> np.ndarray:
 
 
 def _levels_of(parent: np.ndarray) -> np.ndarray:
-    """Level of each node by following parents (inputs are topologically ordered)."""
+    """Level of each node by following parents (inputs are topologically ordered;
+    every root, parent -1, is level 0)."""
     lv = np.zeros(len(parent), np.int64)
     for i in range(1, len(parent)):
-        lv[i] = lv[parent[i]] + 1
+        lv[i] = 0 if parent[i] < 0 else lv[parent[i]] + 1
     return lv
 
 
 def _children_of(parent: np.ndarray):
     ch = [[] for _ in range(len(parent))]
     for i in range(1, len(parent)):
-        ch[int(parent[i])].append(i)
+        if parent[i] >= 0:
+            ch[int(parent[i])].append(i)
     return ch
 
 
@@ -443,18 +445,22 @@ def stochastic_inputs(seed: int, parent: np.ndarray, vocab: int, temperature: fl
     return StochasticInputs(draft=draft, logits=logits, q=q, coins=coins, temperature=float(temperature))
 
 
-def workload_trees(name: str, seed: int, batch: int = 64) -> np.ndarray:
-    """The [B, N] parent arrays of a named workload (the same draws its builder makes)."""
+def workload_trees(name: str, seed: int, batch: int = 64, forest_roots: int = 0) -> np.ndarray:
+    """The [B, N] parent arrays of a named workload (the same draws its builder
+    makes).  With ``forest_roots`` > 0 each sequence is instead a forest of that
+    many trees (``forest_random``) with the same node count and depth."""
     if name == "c1":
+        if forest_roots:
+            raise ValueError("c1 has a fixed tree")
         return tree_worked_example()[None, :]
-    g = rng(seed, "tree")
-    if name == "c2":
-        return tree_random_levels(g, 64, 6)[None, :]
-    if name == "c4":
-        return np.stack([tree_random_levels(g, 64, 8) for _ in range(batch)])
-    if name == "c5":
-        return np.stack([tree_random_levels(g, 192, 10) for _ in range(4)])
-    raise ValueError(f"{name} has no draft tokens to verify")
+    g = rng(seed, "tree" if not forest_roots else f"forest{forest_roots}")
+    shape = {"c2": (1, 64, 6), "c4": (batch, 64, 8), "c5": (4, 192, 10)}
+    if name not in shape:
+        raise ValueError(f"{name} has no draft tokens to verify")
+    B, N, depth = shape[name]
+    if forest_roots:
+        return np.stack([forest_random(g, N, forest_roots, depth) for _ in range(B)])
+    return np.stack([tree_random_levels(g, N, depth) for _ in range(B)])
 
 
 SEEDS = {"c1": 20260001, "c2": 20260002, "c3": 20260003, "c4": 20260004, "c5": 20260005}
@@ -523,12 +529,12 @@ def c1(seed: int = 20260001, **extra) -> Case:
                       permute=False, vocab=1000, plant_len=2, plant_target=[3], **extra)
 
 
-def c2(seed: int = 20260002, vocab: int = 128256, **extra) -> Case:
+def c2(seed: int = 20260002, vocab: int = 128256, forest_roots: int = 0, **extra) -> Case:
     """Llama-3-8B-shaped layer: batch 1, 32 q / 8 kv heads, head_dim 128, contiguous
     4096-token prefix, a random 64-node tree of depth 6.  The workload lists no
     logits for this shape; the verification step here draws them over the
     Llama-3 vocabulary (128256) with a planted accepted length uniform in [0, 6]."""
-    parent = workload_trees("c2", seed)[0]
+    parent = workload_trees("c2", seed, forest_roots=forest_roots)[0]
     plant = int(rng(seed, "plant").integers(0, 7))
     case = build_case("c2", seed, parent, [4096], Hq=32, Hkv=8, D=128, bs=4096, permute=False,
                       vocab=vocab, plant_len=plant, **extra)
@@ -545,22 +551,22 @@ def c3(seed: int = 20260003, **extra) -> Case:
     return build_case("c3", seed, parent, plen, Hq=32, Hkv=8, D=128, bs=16, permute=True, **extra)
 
 
-def c4(seed: int = 20260004, batch: int = 64, **extra) -> Case:
+def c4(seed: int = 20260004, batch: int = 64, forest_roots: int = 0, **extra) -> Case:
     """70B-shaped layer: batch 64, 64 q / 8 kv heads, head_dim 128, paged KV (block 16),
     prefix 8192; per-sequence random 64-node trees of depth 8; logits over 128256
     with planted accepted lengths uniform in [0, 8]."""
-    parents = workload_trees("c4", seed, batch=batch)
+    parents = workload_trees("c4", seed, batch=batch, forest_roots=forest_roots)
     plant = rng(seed, "plant").integers(0, 9, size=batch)
     return build_case("c4", seed, parents, [8192] * batch, Hq=64, Hkv=8, D=128, bs=16,
                       permute=True, vocab=128256, plant_len=plant, **extra)
 
 
-def c5(seed: int = 20260005, prefix: int = 131072, **extra) -> Case:
+def c5(seed: int = 20260005, prefix: int = 131072, forest_roots: int = 0, **extra) -> Case:
     """Long-context wide tree: batch 4, prefix 131072, 32 q / 8 kv heads, head_dim 128,
     paged KV (block 64); a random 192-node tree of depth 10; 1% of key rows scaled by
     8; logits over 128256.  No accepted length is given for this shape; one uniform
     in [0, 10] is planted per sequence so that the walk is exercised."""
-    parents = workload_trees("c5", seed)
+    parents = workload_trees("c5", seed, forest_roots=forest_roots)
     plant = rng(seed, "plant").integers(0, 11, size=4)
     return build_case("c5", seed, parents, [prefix] * 4, Hq=32, Hkv=8, D=128, bs=64,
                       permute=True, vocab=128256, plant_len=plant, hot_key_frac=0.01, **extra)
