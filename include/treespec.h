@@ -177,7 +177,7 @@ TS_API size_t tree_attn_workspace_size(const ts_attn_params* p);
  * call only (calls sharing one workspace must be stream-ordered).
  * Returns TS_ERR_NULL / TS_ERR_SHAPE / TS_ERR_UNSUPPORTED / TS_ERR_WORKSPACE /
  * TS_ERR_CUDA; a block id outside the pool sets status[b] = TS_ERR_BAD_BLOCK
- * (that block is read as zeros), a timed-out internal wait sets
+ * (block 0 is read in its place), a timed-out internal wait sets
  * TS_ERR_TIMEOUT.
  */
 TS_API ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
