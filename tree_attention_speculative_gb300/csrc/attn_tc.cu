@@ -20,8 +20,8 @@
 //   warp 7     TMA loads of the V tiles (paged blocks: one box per block); K
 //              and V each stream through their own 3-stage ring.
 //   warp 5     QK issuer (one thread): S(j) = Q K(j)^T, both operands in
-//              swizzled shared memory, into S buffer j%2 once PV(j-2) (the
-//              last reader of that buffer) has completed (s_free[j%2]).
+//              swizzled shared memory, into S buffer j%3 once PV(j-3) (the
+//              last reader of that buffer) has completed (s_free[j%3]).
 //   warp 6     PV issuer (one thread): O += P(j) V(j), P read from TMEM, V
 //              from shared memory, as soon as the softmax has written P(j).
 //   One thread issues a tcgen05.mma only every ~120-160 cycles, about half
@@ -32,7 +32,9 @@
 // Shared-memory K/V tiles of the prefix are laid out [8-row group][D half]
 // [8 rows x 128 B] (each 1 KB piece one 128-byte-swizzle atom), so one TMA box
 // brings every D column of a paged block; tree tiles are [D half][128 rows].
-// TMEM (512 columns): O at [0, D), S buffers at [128, 256) and [256, 384).
+// TMEM (512 columns): O at [0, D), three S buffers at [128, 256), [256, 384)
+// and [384, 512): QK can run two tiles ahead of the softmax, so the softmax
+// does not wait for the PV that frees the buffer it needs next.
 // Every mbarrier wait is bounded; a timeout sets a shared abort flag, every
 // role winds down, the CTA frees its TMEM and reports TS_ERR_TIMEOUT.
 #include "fastexp.cuh"
@@ -54,6 +56,7 @@ constexpr int V_PRODUCER_WARP = 7;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_O = 0;
 constexpr uint32_t TMEM_S0 = 128;
+constexpr int NSB = 3;  // S buffers in TMEM
 constexpr uint64_t WAIT_LIMIT_NS = 200000000ull;   // 200 ms: far above any legitimate wait
 constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units
 constexpr float NEG_INF = -INFINITY;
@@ -77,9 +80,9 @@ struct __align__(1024) Smem {
   uint64_t v_full[Cfg<D>::NST];
   uint64_t k_empty[Cfg<D>::NST];  // K slot free: its QK completed
   uint64_t v_empty[Cfg<D>::NST];  // V slot free: its PV completed
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t s_free[2];  // S buffer b no longer read: PV of its last tile completed
+  uint64_t s_full[NSB];
+  uint64_t p_full[NSB];
+  uint64_t s_free[NSB];  // S buffer b no longer read: PV of its last tile completed
   uint64_t o_ready;
   uint32_t tmem_base;
   int abort_flag;
@@ -157,7 +160,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       mbar_init(&sm.k_empty[i], 1);
       mbar_init(&sm.v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NSB; ++i) {
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.p_full[i], SOFTMAX_THREADS);
       mbar_init(&sm.s_free[i], 1);
@@ -276,14 +279,14 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       bool ok = wait_bar(&sm.q_full, 0, abort_flag);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int slot = j % C::NST;
-        // K(j) has landed; S buffer j%2 is free once PV(j-2) has completed
+        // K(j) has landed; S buffer j%3 is free once PV(j-3) has completed
         // (a per-buffer barrier: it can never run two completions ahead)
         ok = wait_bar(&sm.k_full[slot], (j / C::NST) & 1, abort_flag) &&
-             (j < 2 || wait_bar(&sm.s_free[j & 1], ((j >> 1) - 1) & 1, abort_flag));
+             (j < NSB || wait_bar(&sm.s_free[j % NSB], ((j / NSB) - 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm.k[slot]);
-        const uint32_t d_tmem = tmem + TMEM_S0 + (j & 1) * 128;
+        const uint32_t d_tmem = tmem + TMEM_S0 + (j % NSB) * 128;
         // prefix tiles: D halves 1 KB apart, 8-row groups HALVES KB apart;
         // tree tiles: D halves 16 KB apart, 8-row groups 1 KB apart
         const bool tree = j >= n_prefix;
@@ -296,7 +299,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
           mma_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + koff, 16, k_sbo), ID_QK,
                  k > 0);
         }
-        mma_commit(&sm.s_full[j & 1]);
+        mma_commit(&sm.s_full[j % NSB]);
         mma_commit(&sm.k_empty[slot]);  // K(j) no longer read
       }
     }
@@ -306,11 +309,11 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       constexpr uint32_t ID_PV = idesc_bf16_f32(128, D, 0, 1);
       for (int j = 0; j < n_tiles; ++j) {
         const int slot = j % C::NST;
-        if (!wait_bar(&sm.p_full[j & 1], (j >> 1) & 1, abort_flag)) break;
+        if (!wait_bar(&sm.p_full[j % NSB], (j / NSB) & 1, abort_flag)) break;
         if (!wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag)) break;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sm.v[slot]);
-        const uint32_t p_tmem = tmem + TMEM_S0 + (j & 1) * 128;
+        const uint32_t p_tmem = tmem + TMEM_S0 + (j % NSB) * 128;
         const bool tree = j >= n_prefix;
         const uint32_t v_lbo = tree ? C::HALF_BYTES : 1024;    // between D halves
         const uint32_t v_sbo = tree ? 1024 : C::HALVES * 1024;  // between 8-key groups
@@ -319,7 +322,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
           mma_ts(tmem + TMEM_O, p_tmem + k * 8, smem_desc_sw128(v_addr + k * 2 * v_sbo, v_lbo, v_sbo), ID_PV,
                  j > 0 || k > 0);
         mma_commit(&sm.o_ready);
-        mma_commit(&sm.s_free[j & 1]);
+        mma_commit(&sm.s_free[j % NSB]);
         mma_commit(&sm.v_empty[slot]);  // V(j) no longer read
         // wait for PV(j) here (every phase in order) and publish the count, so
         // the softmax looks at O only when it has to rescale it
@@ -348,12 +351,12 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     float m_run = NEG_INF, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      if (!__all_sync(0xffffffffu, wait_bar(&sm.s_full[j & 1], (j >> 1) & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, wait_bar(&sm.s_full[j % NSB], (j / NSB) & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t s_tmem = tmem + lane_base + TMEM_S0 + (j & 1) * 128;
+      const uint32_t s_tmem = tmem + lane_base + TMEM_S0 + (j % NSB) * 128;
       float s[KV_TILE];
       {
         // all four TMEM loads in flight before one wait
@@ -487,7 +490,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       l_run += rowsum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sm.p_full[j & 1]);
+      mbar_arrive(&sm.p_full[j % NSB]);
     }
     // epilogue: wait for the last PV, normalise, write
     if (ok && __all_sync(0xffffffffu, wait_count(&sm.pv_done, n_tiles, abort_flag))) {
