@@ -14,7 +14,7 @@
 //
 //   warps 0-3  softmax: thread t owns TMEM lane t = row t.  Loads S from TMEM,
 //              masks, tracks the running max/sum, writes P (bf16) back over S,
-//              rescales O when the max moves by more than 2^8 (exact: the final
+//              rescales O when the max moves by more than 2^20 (exact: the final
 //              normalisation uses the same running max), writes the output.
 //   warp 4     TMEM allocation; TMA loads of the Q tile and of the K tiles
 //   warp 7     TMA loads of the V tiles (paged blocks: one box per block); K
@@ -58,7 +58,13 @@ constexpr uint32_t TMEM_O = 0;
 constexpr uint32_t TMEM_S0 = 128;
 constexpr int NSB = 3;  // S buffers in TMEM
 constexpr uint64_t WAIT_LIMIT_NS = 200000000ull;   // 200 ms: far above any legitimate wait
-constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units
+// O is rescaled only when a row's max rises by more than 2^20 (log2 units).
+// Until then p = 2^(s - m_run) <= 2^20: bf16 P (range to 3e38) and the fp32 O
+// and l accumulators (relative precision independent of scale) stay exact up
+// to rounding, and the final normalisation uses the same running max.  Fewer
+// rescales matter where hot keys move the max often (each rescale waits for
+// the previous PV).
+constexpr float RESCALE_THRESHOLD = 20.0f;
 constexpr float NEG_INF = -INFINITY;
 
 template <int D>
