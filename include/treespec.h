@@ -18,6 +18,8 @@
  *                           the same for several roots per sequence
  *   tree_verify_stochastic  temperature verification by rejection sampling
  *   tree_commit_accepted    append the accepted path to the paged cache
+ *   tree_attn_workspace_size, tree_attn_plan, tree_verify_workspace_size
+ *                           host-only queries: workspace bytes, split plan
  *
  * Sources (web pages on the method):
  *   [P1] "Tree Attention", inferensys glossary.
@@ -161,6 +163,20 @@ typedef struct ts_attn_params {
  * Returns 0 for arguments tree_attn_fwd would reject.
  */
 TS_API size_t tree_attn_workspace_size(const ts_attn_params* p);
+
+/*
+ * tree_attn_plan — how tree_attn_fwd will cut the work for these arguments
+ * (host only, launches nothing).  The prefix of every (sequence, KV head,
+ * 128-row tile) is cut into splits of *chunk_tiles 128-token tiles;
+ * *max_splits is the split count of the longest sequence (the grid's split
+ * extent), and *tree_split is 1 when the tree block runs as a split of its
+ * own rather than on the last prefix split.  With *max_splits == 1 the
+ * attention kernel writes `out` itself; otherwise the splits' partials are
+ * merged by a second kernel.  Each output pointer may be NULL.
+ * Returns TS_ERR_NULL / TS_ERR_SHAPE / TS_ERR_UNSUPPORTED like tree_attn_fwd.
+ */
+TS_API ts_status tree_attn_plan(const ts_attn_params* p, int32_t* chunk_tiles, int32_t* max_splits,
+                                int32_t* tree_split);
 
 /*
  * tree_attn_fwd — the attention layer of the batched verification pass

@@ -3,6 +3,24 @@ run one verification step through the library's C ABI."""
 import numpy as np
 import torch
 
+# Attention cases compared element by element with the oracle:
+# name, B, N, Hq, Hkv, D, prefix lengths, block size, tree kind.  Between them
+# they take every layout the split planner can choose (tests/test_abi_host.py
+# checks that): one split per unit (the kernel writes the output itself), the
+# tree block on the last prefix split, and the tree block on a split of its own.
+SMALL = [
+    ("g4_ragged", 2, 37, 8, 2, 128, [0, 300], 16, "random"),
+    ("g1_d64", 1, 5, 2, 2, 64, [16], 16, "worked"),
+    ("g2_multi_tile", 3, 70, 4, 2, 128, [129, 1, 640], 32, "levels"),
+    ("g8_rows_over_tile", 2, 40, 16, 2, 128, [257, 96], 64, "random"),
+    ("g16", 1, 9, 16, 1, 64, [383], 128, "chain"),
+    ("w3_192_nodes", 1, 192, 2, 1, 128, [200], 16, "levels"),
+    ("w4_256_nodes", 1, 256, 1, 1, 64, [0], 16, "random"),
+    ("contiguous_2k", 2, 26, 8, 2, 128, [2048, 2048], 2048, "widths"),
+    ("tree_on_last_split", 5, 130, 8, 8, 128, [3000, 2963, 2926, 2889, 2852], 16, "levels"),
+    ("one_split_per_unit", 16, 26, 32, 8, 128, [1500 - 37 * i for i in range(16)], 16, "widths"),
+]
+
 ATOL = 1e-2   # |out - ref| <= ATOL + RTOL * |ref| for bf16 attention outputs
 RTOL = 1e-2
 LSE_ATOL = 1e-3

@@ -60,8 +60,8 @@ class _FakeTensor:
 
 
 def _params(ts, B=2, N=26, Hq=32, Hkv=8, D=128, bs=16, P=(1000, 3000), **kw):
-    nblk = sum(-(-p // bs) for p in P)
-    maxb = max(-(-p // bs) for p in P)
+    nblk = max(1, sum(-(-p // bs) for p in P))
+    maxb = max(1, max(-(-p // bs) for p in P))
     f = _FakeTensor
     args = dict(q=f((B, N, Hq, D)), k_cache=f((nblk, Hkv, bs, D)), v_cache=f((nblk, Hkv, bs, D)),
                 block_table=f((B, maxb)), prefix_len=f((B,)), prefix_len_host=np.array(P, np.int32),
@@ -75,8 +75,34 @@ def test_attn_workspace_query_and_plan(ts):
     p = _params(ts)
     n = ts.tree_attn_workspace_size(p)
     assert n > 0 and n % 256 == 0
-    # partial outputs for at least one split of every output row
-    assert n >= 2 * 26 * 32 * 128 * 4
+    # bf16 partial outputs of at least two splits of every output row
+    assert n >= 2 * 26 * 32 * 128 * 2
+
+
+def test_attn_plan_query(ts):
+    p = _params(ts)
+    plan = ts.tree_attn_plan(p)
+    assert plan["chunk_tiles"] >= 1 and plan["max_splits"] >= 1 and plan["tree_split"] in (0, 1)
+    assert ts.lib().tree_attn_plan(ctypes.byref(p), None, None, None) == 0
+    bad = _params(ts, D=96)
+    assert ts.lib().tree_attn_plan(ctypes.byref(bad), None, None, None) == -4
+
+
+def _plan_of(ts, name, B, N, Hq, Hkv, D, plens, bs, tree):
+    return ts.tree_attn_plan(_params(ts, B=B, N=N, Hq=Hq, Hkv=Hkv, D=D, bs=bs, P=tuple(plens)))
+
+
+def test_small_parity_cases_cover_every_split_layout(ts):
+    """The element-wise GPU parity cases must exercise each kernel layout."""
+    from tests.gpu_util import SMALL
+    layouts = set()
+    for spec in SMALL:
+        plan = _plan_of(ts, *spec)
+        if plan["max_splits"] == 1:
+            layouts.add("direct")
+        else:
+            layouts.add("tree split" if plan["tree_split"] else "tree on last prefix split")
+    assert layouts == {"direct", "tree split", "tree on last prefix split"}
 
 
 @pytest.mark.parametrize("change,code", [

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.gpu_util import LSE_ATOL, assert_close_attention, out_f64, run_case, to_dev
+from tests.gpu_util import SMALL, LSE_ATOL, assert_close_attention, out_f64, run_case, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -70,19 +70,6 @@ def test_ancestry_worked_example_and_invalid_trees():
 
 
 # --------------------------------------------------------------------------- attention
-
-SMALL = [
-    # name, B, N, Hq, Hkv, D, prefixes, bs, tree
-    ("g4_ragged", 2, 37, 8, 2, 128, [0, 300], 16, "random"),
-    ("g1_d64", 1, 5, 2, 2, 64, [16], 16, "worked"),
-    ("g2_multi_tile", 3, 70, 4, 2, 128, [129, 1, 640], 32, "levels"),
-    ("g8_rows_over_tile", 2, 40, 16, 2, 128, [257, 96], 64, "random"),
-    ("g16", 1, 9, 16, 1, 64, [383], 128, "chain"),
-    ("w3_192_nodes", 1, 192, 2, 1, 128, [200], 16, "levels"),
-    ("w4_256_nodes", 1, 256, 1, 1, 64, [0], 16, "random"),
-    ("contiguous_2k", 2, 26, 8, 2, 128, [2048, 2048], 2048, "widths"),
-]
-
 
 def _small_case(name, B, N, Hq, Hkv, D, plens, bs, tree):
     g = W.rng(len(name), name)

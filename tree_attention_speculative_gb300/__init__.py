@@ -20,7 +20,7 @@ from ._build import LIB as LIB_PATH
 
 __all__ = [
     "TreeSpecError", "lib", "ts_status_str", "tree_build_ancestry", "AttnParams", "attn_params",
-    "tree_attn_workspace_size", "tree_attn_fwd", "tree_verify_workspace_size", "tree_verify_greedy",
+    "tree_attn_workspace_size", "tree_attn_plan", "tree_attn_fwd", "tree_verify_workspace_size", "tree_verify_greedy",
     "tree_verify_greedy_noalloc", "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic",
     "tree_build_ancestry_forest", "tree_verify_greedy_forest", "NOALLOC_SCRATCH_BYTES",
     "STATUS",
@@ -54,7 +54,7 @@ class AttnParams(ctypes.Structure):
 _LIB: Optional[ctypes.CDLL] = None
 
 # every symbol include/treespec.h declares
-EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_fwd",
+EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_plan", "tree_attn_fwd",
            "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc",
            "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic", "tree_build_ancestry_forest",
            "tree_verify_greedy_forest")
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.tree_build_ancestry.restype = i32
         L.tree_attn_workspace_size.argtypes = [ctypes.POINTER(AttnParams)]
         L.tree_attn_workspace_size.restype = sz
+        L.tree_attn_plan.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp]
+        L.tree_attn_plan.restype = i32
         L.tree_attn_fwd.argtypes = [ctypes.POINTER(AttnParams), vp, sz, vp]
         L.tree_attn_fwd.restype = i32
         L.tree_verify_workspace_size.argtypes = [i32, i32, i32]
@@ -161,6 +163,14 @@ def attn_params(q, k_cache, v_cache, block_table, prefix_len, prefix_len_host, k
 
 def tree_attn_workspace_size(params: AttnParams) -> int:
     return int(lib().tree_attn_workspace_size(ctypes.byref(params)))
+
+
+def tree_attn_plan(params: AttnParams) -> dict:
+    """The split plan tree_attn_fwd uses for these arguments (host only)."""
+    c, s, t = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().tree_attn_plan(ctypes.byref(params), ctypes.byref(c), ctypes.byref(s), ctypes.byref(t)),
+           "tree_attn_plan")
+    return {"chunk_tiles": c.value, "max_splits": s.value, "tree_split": t.value}
 
 
 def tree_attn_fwd(params: AttnParams, workspace: torch.Tensor, stream=None) -> None:

@@ -26,6 +26,7 @@ k_ancestry(const int32_t* __restrict__ parent, const int32_t* __restrict__ prefi
   const int i = threadIdx.x;
   pdl_wait();
   pdl_trigger();
+  const int P = prefix_len[b];  // loaded beside the parents, not after the walk
   int p = -1;
   bool ok = true;
   if (i < N) {
@@ -59,7 +60,7 @@ k_ancestry(const int32_t* __restrict__ parent, const int32_t* __restrict__ prefi
     if (W > 2) row[2] = w2;
     if (W > 3) row[3] = w3;
     depth[(size_t)b * N + i] = d;
-    pos[(size_t)b * N + i] = valid ? prefix_len[b] + d : 0;
+    pos[(size_t)b * N + i] = valid ? P + d : 0;
   }
   if (i == 0) status[b] = valid ? TS_OK : TS_ERR_BAD_TREE;
 }

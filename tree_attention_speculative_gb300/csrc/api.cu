@@ -43,13 +43,17 @@ ts_status check_attn(const ts_attn_params* p) {
 }
 
 // Split plan.  Every (unit, row tile) is one chain of 128-token KV tiles; a
-// split cuts the chain into CTAs of `chunk_tiles` tiles (the last one of a
-// unit also runs the tree block).  The attention kernel holds one CTA per SM,
+// split cuts the chain into CTAs of `chunk_tiles` tiles.  The tree block rides
+// on the last prefix split of a unit, or (tree_split) on a CTA of its own that
+// runs beside the prefix splits.  The attention kernel holds one CTA per SM,
 // so the time of a plan is about
-//     waves * (chunk + per-CTA overhead) + cost of the split partials,
+//     waves * (chunk + per-CTA overhead) [+ tree tiles] + cost of the partials,
 // in units of one tile's work on one SM (about 0.5 us).  The partials are
-// written and read back once (fp32 O + lse per split), priced at the
-// measured HBM rate.  The plan with the smallest estimate wins.
+// written and read back once (bf16 O + fp32 lse per split, about 2D + 4 bytes
+// a row) and priced at twice those bytes at the measured HBM rate: at the
+// plain price the planner picked 7 splits for the batched-serving workload
+// (16 sequences, paged prefixes of 1-16K), which ran 5% slower than 4.  The plan with the smallest estimate wins; ties keep the
+// tree on the last prefix split.
 AttnPlan plan_attn(const ts_attn_params* p) {
   AttnPlan pl{};
   const int G = p->Hq / p->Hkv;
@@ -64,34 +68,38 @@ AttnPlan plan_attn(const ts_attn_params* p) {
   const double tile_bytes_equiv = 3.6e6;  // HBM bytes moved in one tile-time
   const double cta_overhead = 1.5;        // prologue + epilogue, in tile-times
   double best = 1e300;
-  int best_chunk = max_tiles;
-  for (int s = 1; s <= 256; ++s) {
-    const int chunk = ceil_div(max_tiles, s);
-    if (s > 1 && chunk == ceil_div(max_tiles, s - 1)) continue;
-    long long ctas = 0;
-    int splits = 1;
-    for (int b = 0; b < p->B; ++b) {
-      const int ns = num_splits(p->prefix_len_host[b], chunk);
-      ctas += (long long)ns * p->Hkv * pl.row_tiles;
-      splits = ns > splits ? ns : splits;
+  int best_chunk = max_tiles, best_ts = 0;
+  for (int ts = 0; ts <= 1; ++ts) {
+    for (int s = 1; s <= 256; ++s) {
+      const int chunk = ceil_div(max_tiles, s);
+      if (s > 1 && chunk == ceil_div(max_tiles, s - 1)) continue;
+      long long ctas = 0;
+      int splits = 1;
+      for (int b = 0; b < p->B; ++b) {
+        const int ns = num_splits(p->prefix_len_host[b], chunk, ts);
+        ctas += (long long)ns * p->Hkv * pl.row_tiles;
+        splits = ns > splits ? ns : splits;
+      }
+      const double waves = (double)((ctas + PLAN_SMS - 1) / PLAN_SMS);
+      double cost = waves * (chunk + cta_overhead) + (ts ? 0 : tree_tiles);
+      if (splits > 1) cost += 2.0 * splits * rows * 2.0 * (p->D * 2.0 + 4.0) / tile_bytes_equiv;
+      if (cost < best) {
+        best = cost;
+        best_chunk = chunk;
+        best_ts = ts;
+      }
+      if (chunk == 1) break;
     }
-    const double waves = (double)((ctas + PLAN_SMS - 1) / PLAN_SMS);
-    double cost = waves * (chunk + cta_overhead) + tree_tiles;
-    if (splits > 1) cost += 2.0 * splits * rows * (p->D + 1) * 4.0 / tile_bytes_equiv;
-    if (cost < best) {
-      best = cost;
-      best_chunk = chunk;
-    }
-    if (chunk == 1) break;
   }
   pl.chunk_tiles = best_chunk;
+  pl.tree_split = best_ts;
   pl.max_splits = 1;
   for (int b = 0; b < p->B; ++b) {
-    const int ns = num_splits(p->prefix_len_host[b], pl.chunk_tiles);
+    const int ns = num_splits(p->prefix_len_host[b], pl.chunk_tiles, pl.tree_split);
     pl.max_splits = ns > pl.max_splits ? ns : pl.max_splits;
   }
   const size_t nrows = (size_t)p->B * p->N * p->Hq;
-  pl.part_o_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * p->D * sizeof(float)) : 0;
+  pl.part_o_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * p->D * 2) : 0;
   pl.part_lse_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * sizeof(float)) : 0;
   pl.workspace_bytes = pl.part_o_bytes + pl.part_lse_bytes;
   if (pl.workspace_bytes == 0) pl.workspace_bytes = 256;  // keep a non-empty workspace contract
@@ -213,6 +221,17 @@ size_t tree_attn_workspace_size(const ts_attn_params* p) {
   return plan_attn(p).workspace_bytes;
 }
 
+ts_status tree_attn_plan(const ts_attn_params* p, int32_t* chunk_tiles, int32_t* max_splits,
+                         int32_t* tree_split) {
+  const ts_status st = check_attn(p);
+  if (st != TS_OK) return st;
+  const AttnPlan pl = plan_attn(p);
+  if (chunk_tiles) *chunk_tiles = pl.chunk_tiles;
+  if (max_splits) *max_splits = pl.max_splits;
+  if (tree_split) *tree_split = pl.tree_split;
+  return TS_OK;
+}
+
 ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
                         ts_stream stream) {
   ts_status st = check_attn(p);
@@ -233,7 +252,7 @@ ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspa
   a.lse = p->lse;
   a.status = p->status;
   char* ws = static_cast<char*>(workspace);
-  a.part_o = reinterpret_cast<float*>(ws);
+  a.part_o = reinterpret_cast<__nv_bfloat16*>(ws);
   a.part_lse = reinterpret_cast<float*>(ws + pl.part_o_bytes);
   a.B = p->B; a.N = p->N; a.Hq = p->Hq; a.Hkv = p->Hkv; a.G = p->Hq / p->Hkv; a.D = p->D;
   a.W = ceil_div(p->N, 64);
@@ -242,6 +261,7 @@ ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspa
   a.scale_log2 = scale * 1.4426950408889634f;
   a.chunk_tiles = pl.chunk_tiles;
   a.max_splits = pl.max_splits;
+  a.tree_split = pl.tree_split;
   a.row_tiles = pl.row_tiles;
   cudaStream_t s = (cudaStream_t)stream;
   if (prepare_device() != cudaSuccess) return TS_ERR_CUDA;

@@ -15,7 +15,10 @@
 //   warps 0-3  softmax: thread t owns TMEM lane t = row t.  Loads S from TMEM,
 //              masks, tracks the running max/sum, writes P (bf16) back over S,
 //              rescales O when the max moves by more than 2^20 (exact: the final
-//              normalisation uses the same running max), writes the output.
+//              normalisation uses the same running max).  At the end each
+//              thread normalises its row of O to bf16 in the idle K ring, in
+//              the 128-byte-swizzled layout of a TMA box, and one thread
+//              stores the boxes: the output itself, or this split's partial.
 //   warp 4     TMEM allocation; TMA loads of the Q tile and of the K tiles
 //   warp 7     TMA loads of the V tiles (paged blocks: one box per block); K
 //              and V each stream through their own 3-stage ring.
@@ -35,6 +38,8 @@
 // TMEM (512 columns): O at [0, D), three S buffers at [128, 256), [256, 384)
 // and [384, 512): QK can run two tiles ahead of the softmax, so the softmax
 // does not wait for the PV that frees the buffer it needs next.
+// The tree block rides on the last prefix split of a unit or, when the host
+// plans it so, on a split of its own that runs beside the prefix splits.
 // Every mbarrier wait is bounded; a timeout sets a shared abort flag, every
 // role winds down, the CTA frees its TMEM and reports TS_ERR_TIMEOUT.
 #include "fastexp.cuh"
@@ -145,7 +150,8 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tm_q,
           const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
-          const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
+          const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
+          const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_po) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -180,19 +186,40 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
+  // the tensor maps are kernel parameters: fetch them before the wait
+  if (warp == PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_vc);
+    tma_prefetch_desc(&tm_kt);
+    tma_prefetch_desc(&tm_vt);
+  }
   // everything above touched no global memory and overlaps the previous
   // kernel's tail; wait for it before reading any input.  The next kernel is
-  // released only at this CTA's teardown: this kernel can run many waves, and
-  // the next kernel's CTAs should not wait on SMs the later waves need.
+  // released only at this CTA's teardown (released at the start, its CTAs
+  // were measured to delay this kernel's first loads by about 2 us).
   pdl_wait();
+  const int t_begin = split * a.chunk_tiles;
+  const int boxes = KV_TILE / args.box_rows;  // boxes (paged blocks) per tile (1 .. 8)
+  const int tpg = 32 / boxes;                 // tiles per group of block-table entries
+  const int* table_row = a.block_table + (size_t)b * a.max_blocks;
+  const int p_dev = a.prefix_len[b];
+  // The producers fetch their first group of block-table entries before the
+  // prefix length is known (index clamped to the table's row), so that the
+  // two loads overlap; entries past the prefix are discarded below.
+  int blk_first = 0;
+  if ((warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && a.max_blocks > 0) {
+    const long long t0 = (long long)(t_begin + lane / boxes) * KV_TILE + (lane % boxes) * args.box_rows;
+    const long long idx = t0 / a.bs;
+    blk_first = table_row[idx < a.max_blocks ? idx : a.max_blocks - 1];
+  }
   int P;
-  const bool p_ok = usable_prefix(a.prefix_len[b], a.chunk_tiles, a.max_splits, a.bs, a.max_blocks, &P);
+  const bool p_ok = usable_prefix(p_dev, a.chunk_tiles, a.max_splits, a.tree_split, a.bs, a.max_blocks, &P);
   const int tiles = prefix_tiles(P);
-  const int ns = num_splits(P, a.chunk_tiles);
+  const int ns = num_splits(P, a.chunk_tiles, a.tree_split);
   const bool has_work = split < ns;  // splits past this sequence's prefix have nothing to do
   if (!p_ok && threadIdx.x == 0 && rt == 0 && split == 0 && a.status) a.status[b] = TS_ERR_SHAPE;
-  const int t_begin = split * a.chunk_tiles;
-  const int n_prefix = min(tiles, t_begin + a.chunk_tiles) - t_begin;
+  const int n_prefix = max(0, min(tiles, t_begin + a.chunk_tiles) - t_begin);
   const int n_tree = (split == ns - 1) ? ceil_div(a.N, KV_TILE) : 0;
   const int n_tiles = n_prefix + n_tree;
 
@@ -207,19 +234,16 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     const CUtensorMap* tm_node = is_v ? &tm_vt : &tm_kt;
     uint64_t* full = is_v ? sm.v_full : sm.k_full;
     uint64_t* empty = is_v ? sm.v_empty : sm.k_empty;
-    const int boxes = KV_TILE / args.box_rows;  // boxes (paged blocks) per tile (1 .. 8)
     const uint32_t box_bytes = args.box_rows * D * 2;
     // Block-table entries are software-pipelined: lane L holds the entry of
     // box (L % boxes) of tile (L / boxes) of a group of 32/boxes tiles; the
     // next group is loaded (one coalesced read) when the current one starts,
     // so the table's load latency hides behind several tiles of TMA issue.
-    const int tpg = 32 / boxes;
-    const int* table_row = a.block_table + (size_t)b * a.max_blocks;
     auto load_group = [&](int grp) -> int {
       const int tile = grp * tpg + lane / boxes;
       const int t0 = (t_begin + tile) * KV_TILE + (lane % boxes) * args.box_rows;
       if (tile >= n_prefix || t0 >= P) return 0;
-      int blk = table_row[t0 / a.bs];
+      int blk = grp == 0 ? blk_first : table_row[t0 / a.bs];
       if (blk < 0 || blk >= a.num_blocks) {
         if (a.status) a.status[b] = TS_ERR_BAD_BLOCK;
         blk = 0;  // read a valid block instead; the sequence is reported as failed
@@ -264,11 +288,6 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   } else if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_kc);
-      tma_prefetch_desc(&tm_vc);
-      tma_prefetch_desc(&tm_kt);
-      tma_prefetch_desc(&tm_vt);
       mbar_arrive_expect_tx(&sm.q_full, C::Q_BYTES);
       const int nodes_per_tile = ROW_TILE / a.G;
       for (int h = 0; h < C::HALVES; ++h)
@@ -498,40 +517,58 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       tc_fence_before();
       mbar_arrive(&sm.p_full[j % NSB]);
     }
-    // epilogue: wait for the last PV, normalise, write
-    if (ok && __all_sync(0xffffffffu, wait_count(&sm.pv_done, n_tiles, abort_flag))) {
+    // epilogue: wait for the last PV, normalise, stage the rows in shared
+    // memory as TMA boxes (128-byte rows, 16-byte chunk k of row r at
+    // k ^ (r % 8): the 128-byte swizzle, and conflict-free for these writes),
+    // then one thread stores the boxes.  The K ring is idle by now: every QK
+    // has completed before the last PV could start.
+    const bool epi = ok && __all_sync(0xffffffffu, wait_count(&sm.pv_done, n_tiles, abort_flag));
+    uint8_t* stage = &sm.k[0][0];
+    float lse2 = 0.f;
+    if (epi) {
       tc_fence_after();
       const float inv = 1.f / l_run;
-      const float lse2 = m_run + __log2f(l_run);
-      const size_t orow = ((size_t)b * a.N + node) * a.Hq + h;
-#pragma unroll
+      lse2 = m_run + __log2f(l_run);
+      // bf16 boxes of 64 columns (one per D half), each 128 rows of 128
+      // bytes; columns c .. c+31 are chunks (c % 64) / 8 .. +3 of box c / 64.
+      // The loop is kept rolled: unrolled, it changed how the softmax loop
+      // above was compiled, which then ran 10% slower on long prefixes.
+#pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t u[32];
         tmem_ld32(tmem + lane_base + TMEM_O + c, u);
         tmem_ld_wait();
-        if (active) {
-          if (args.direct) {
-            uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + c);
+        uint8_t* row = stage + (c / 64) * (ROW_TILE * 128) + r * 128;
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(u[e + 0]) * inv, __uint_as_float(u[e + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(u[e + 2]) * inv, __uint_as_float(u[e + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(u[e + 4]) * inv, __uint_as_float(u[e + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(u[e + 6]) * inv, __uint_as_float(u[e + 7]) * inv);
-              dst[e / 8] = v;
-            }
-          } else {
-            const size_t rows = (size_t)a.B * a.N * a.Hq;
-            float4* dst = reinterpret_cast<float4*>(a.part_o + (size_t)split * rows * D + orow * D + c);
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              dst[e / 4] = make_float4(__uint_as_float(u[e]) * inv, __uint_as_float(u[e + 1]) * inv,
-                                       __uint_as_float(u[e + 2]) * inv, __uint_as_float(u[e + 3]) * inv);
-          }
+        for (int q = 0; q < 4; ++q) {
+          const int k = (c % 64) / 8 + q;
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(u[8 * q + 0]) * inv, __uint_as_float(u[8 * q + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(u[8 * q + 2]) * inv, __uint_as_float(u[8 * q + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(u[8 * q + 4]) * inv, __uint_as_float(u[8 * q + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(u[8 * q + 6]) * inv, __uint_as_float(u[8 * q + 7]) * inv);
+          *reinterpret_cast<uint4*>(row + ((k ^ (r & 7)) << 4)) = v;
         }
       }
+      fence_proxy_async();
+    }
+    // every softmax thread reaches this barrier, whatever happened above
+    const bool all_epi = named_barrier_and(1, SOFTMAX_THREADS, epi);
+    if (all_epi) {
+      if (threadIdx.x == 0) {
+        // rows of nodes >= N fall outside the tensor and are not written
+        const int node0 = rt * (ROW_TILE / a.G);
+        for (int hh = 0; hh < C::HALVES; ++hh) {
+          if (args.direct)
+            tma_store_4d(&tm_o, stage + hh * (ROW_TILE * 128), 64 * hh, g * a.G, node0, b);
+          else
+            tma_store_5d(&tm_po, stage + hh * (ROW_TILE * 128), 64 * hh, g * a.G, node0, b, split);
+        }
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
       if (active) {
+        const size_t orow = ((size_t)b * a.N + node) * a.Hq + h;
         if (args.direct) {
           if (a.lse) a.lse[orow] = lse2 * 0.69314718055994531f;
         } else {
@@ -588,8 +625,26 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
     if (!encode_bf16_sw128(&m_kt, a.k_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
     if (!encode_bf16_sw128(&m_vt, a.v_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
+  // output boxes of 64 columns: bf16 out [B, N, Hq, D] like q (direct), or the
+  // bf16 partial of each split [max_splits, B, N, Hq, D]
+  CUtensorMap m_o, m_po;
+  std::memset(&m_o, 0, sizeof(m_o));
+  std::memset(&m_po, 0, sizeof(m_po));
+  if (t.direct) {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.N, (uint64_t)a.B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)a.Hq * D * 2, (uint64_t)a.N * a.Hq * D * 2};
+    const uint32_t box[4] = {64, (uint32_t)a.G, (uint32_t)(ROW_TILE / a.G), 1};
+    if (!encode_bf16_sw128(&m_o, a.out, 4, dims, str, box)) return cudaErrorInvalidValue;
+  } else {
+    const uint64_t dims[5] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.N, (uint64_t)a.B, (uint64_t)a.max_splits};
+    const uint64_t str[4] = {(uint64_t)D * 2, (uint64_t)a.Hq * D * 2, (uint64_t)a.N * a.Hq * D * 2,
+                             (uint64_t)a.B * a.N * a.Hq * D * 2};
+    const uint32_t box[5] = {64, (uint32_t)a.G, (uint32_t)(ROW_TILE / a.G), 1, 1};
+    if (!encode_bf16_sw128(&m_po, a.part_o, 5, dims, str, box)) return cudaErrorInvalidValue;
+  }
   dim3 grid(a.row_tiles, a.max_splits, a.B * a.Hkv);
-  return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt);
+  return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt, m_o,
+                    m_po);
 }
 
 }  // namespace

@@ -3,84 +3,115 @@
 // The verification pass of [P1] Key Mechanisms > Batched Parallel Verification
 // is one softmax over all keys a node sees.  The prefix is cut into splits so
 // that enough CTAs share the work; each split s leaves a normalised partial
-// O_s and its base-2 log-sum-exp L_s.  The exact softmax over the union is
+// O_s (bf16, the output's type) and its base-2 log-sum-exp L_s (fp32).  The exact softmax over the union is
 //     out = sum_s 2^(L_s - M) O_s / sum_s 2^(L_s - M),  M = max_s L_s,
 //     lse = ln 2 * (M + log2 sum_s 2^(L_s - M)).
-// One warp per output row (b, node, head); each lane owns D/32 consecutive
-// channels, so partial reads and the bf16 store are coalesced.
+// D/8 lanes per output row (b, node, head): each lane owns 8 consecutive
+// channels, so every partial read and the output store is one 16-byte access
+// per lane and a warp merges 32/(D/8) rows at once.  The splits are taken in
+// groups of eight: a group's lse and O loads are all in flight at once (the
+// first group's are issued together with the prefix-length load, for every
+// split the workspace holds, and the ones past this sequence's split count
+// are dropped), and a running maximum rescales the sums between groups.
+// 128-thread blocks so that a block fits beside an attention CTA.
 #include "internal.cuh"
 
 namespace ts {
 
+constexpr int COMBINE_THREADS = 128;
+constexpr int COMBINE_GROUP = 8;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+    f[2 * k] = t.x;
+    f[2 * k + 1] = t.y;
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(COMBINE_THREADS)
 k_combine(AttnArgs a) {
-  constexpr int PER = D / 32;
+  constexpr int LPR = D / 8;                        // lanes per row
+  constexpr int ROWS_PER_BLOCK = COMBINE_THREADS / LPR;
   const int rows = a.B * a.N * a.Hq;
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * ROWS_PER_BLOCK + (int)threadIdx.x / LPR;
+  const int sub = (int)threadIdx.x % LPR;          // channels 8*sub .. 8*sub+7
   pdl_wait();
   pdl_trigger();
   if (row >= rows) return;
   const int b = row / (a.N * a.Hq);
-  int P;
-  usable_prefix(a.prefix_len[b], a.chunk_tiles, a.max_splits, a.bs, a.max_blocks, &P);
-  const int ns = num_splits(P, a.chunk_tiles);
   const size_t stride_lse = (size_t)rows;
   const size_t stride_o = (size_t)rows * D;
 
-  // every split's lse in flight at once: lane s holds split s (then s+32, ...)
-  float m = -INFINITY;
-  for (int s = lane; s < ns; s += 32) m = fmaxf(m, a.part_lse[s * stride_lse + row]);
+  float w[COMBINE_GROUP];
+  uint4 raw[COMBINE_GROUP];
+  auto load_group = [&](int s0, int limit) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float acc[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  float den = 0.f;
-  // partial rows: up to 8 independent loads in flight per lane
-  for (int s0 = 0; s0 < ns; s0 += 8) {
-    float w[8];
-    float v[8][PER];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < COMBINE_GROUP; ++i) {
       const int s = s0 + i;
-      w[i] = 0.f;
-      if (s < ns) {
+      w[i] = -INFINITY;
+      raw[i] = make_uint4(0, 0, 0, 0);
+      if (s < limit) {
         w[i] = a.part_lse[s * stride_lse + row];
-        const float* o = a.part_o + s * stride_o + (size_t)row * D + lane * PER;
-        if constexpr (PER == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(o);
-          v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
-        } else {
-          const float2 x = *reinterpret_cast<const float2*>(o);
-          v[i][0] = x.x; v[i][1] = x.y;
-        }
+        raw[i] = *reinterpret_cast<const uint4*>(a.part_o + s * stride_o + (size_t)row * D + sub * 8);
       }
     }
+  };
+  const int p_dev = a.prefix_len[b];
+  load_group(0, a.max_splits);
+  int P;
+  usable_prefix(p_dev, a.chunk_tiles, a.max_splits, a.tree_split, a.bs, a.max_blocks, &P);
+  const int ns = num_splits(P, a.chunk_tiles, a.tree_split);
+
+  float m = -INFINITY, den = 0.f;
+  float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+  for (int s0 = 0; s0 < ns; s0 += COMBINE_GROUP) {
+    if (s0 > 0) load_group(s0, ns);
+    float gm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < COMBINE_GROUP; ++i)
+      if (s0 + i < ns) gm = fmaxf(gm, w[i]);
+    const float m_new = fmaxf(m, gm);
+    const float f = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
+    den *= f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] *= f;
+    m = m_new;
+#pragma unroll
+    for (int i = 0; i < COMBINE_GROUP; ++i) {
       if (s0 + i < ns) {
         const float wi = exp2f(w[i] - m);
         den += wi;
+        float v[8];
+        bf16x8_to_f32(raw[i], v);
 #pragma unroll
-        for (int k = 0; k < PER; ++k) acc[k] = fmaf(wi, v[i][k], acc[k]);
+        for (int k = 0; k < 8; ++k) acc[k] = fmaf(wi, v[k], acc[k]);
       }
     }
   }
   const float inv = 1.f / den;
-  __nv_bfloat16* dst = a.out + (size_t)row * D + lane * PER;
+  uint4 o;
+  uint32_t* ow = &o.x;
 #pragma unroll
-  for (int k = 0; k < PER; k += 2)
-    *reinterpret_cast<__nv_bfloat162*>(dst + k) = __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
-  if (a.lse && lane == 0) a.lse[row] = (m + log2f(den)) * 0.69314718055994531f;
+  for (int k = 0; k < 4; ++k) {
+    const __nv_bfloat162 t = __floats2bfloat162_rn(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+    ow[k] = *reinterpret_cast<const uint32_t*>(&t);
+  }
+  *reinterpret_cast<uint4*>(a.out + (size_t)row * D + sub * 8) = o;
+  if (a.lse && sub == 0) a.lse[row] = (m + log2f(den)) * 0.69314718055994531f;
 }
 
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s) {
   const int rows = a.B * a.N * a.Hq;
-  const int grid = ceil_div(rows, 8);
-  return a.D == 128 ? launch_pdl(k_combine<128>, dim3(grid), dim3(256), 0, s, a)
-                   : launch_pdl(k_combine<64>, dim3(grid), dim3(256), 0, s, a);
+  const int per_block = COMBINE_THREADS / (a.D / 8);
+  const int grid = ceil_div(rows, per_block);
+  return a.D == 128 ? launch_pdl(k_combine<128>, dim3(grid), dim3(COMBINE_THREADS), 0, s, a)
+                   : launch_pdl(k_combine<64>, dim3(grid), dim3(COMBINE_THREADS), 0, s, a);
 }
 
 }  // namespace ts

@@ -45,13 +45,14 @@ constexpr int PLAN_SMS = 152;  // GB300: the planner sizes grids for 152 SMs
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Number of prefix tiles of a sequence, and how many splits its prefix is cut
-// into when every split takes `chunk_tiles` tiles.  A sequence with no prefix
-// still has one split: it carries the tree block.  The tree block always rides
-// on the LAST split of a sequence.
+// into when every split takes `chunk_tiles` tiles.  The tree block rides on
+// the LAST split of a sequence: with tree_split = 0 that is the last prefix
+// split (a sequence with no prefix still has one split for it); with
+// tree_split = 1 it is one more split of its own, with no prefix tiles.
 __host__ __device__ inline int prefix_tiles(int P) { return ceil_div(P, KV_TILE); }
-__host__ __device__ inline int num_splits(int P, int chunk_tiles) {
-  int t = prefix_tiles(P);
-  return t == 0 ? 1 : ceil_div(t, chunk_tiles);
+__host__ __device__ inline int num_splits(int P, int chunk_tiles, int tree_split) {
+  const int ps = ceil_div(prefix_tiles(P), chunk_tiles);
+  return tree_split ? ps + 1 : (ps == 0 ? 1 : ps);
 }
 
 // The prefix length a kernel may use for sequence b: the device value, clamped
@@ -59,9 +60,9 @@ __host__ __device__ inline int num_splits(int P, int chunk_tiles) {
 // width.  Returns true when no clamping was needed.  Kernels report a clamp as
 // TS_ERR_SHAPE so a disagreement between the device and host prefix lengths can
 // never drive an access outside the planned buffers.
-__host__ __device__ inline bool usable_prefix(int P, int chunk_tiles, int max_splits, int bs, int max_blocks,
-                                              int* out) {
-  long long cap = (long long)chunk_tiles * max_splits * KV_TILE;
+__host__ __device__ inline bool usable_prefix(int P, int chunk_tiles, int max_splits, int tree_split, int bs,
+                                              int max_blocks, int* out) {
+  long long cap = (long long)chunk_tiles * (max_splits - tree_split) * KV_TILE;
   const long long cap_blocks = (long long)max_blocks * bs;
   if (cap_blocks < cap) cap = cap_blocks;
   long long v = P < 0 ? 0 : P;
@@ -84,19 +85,21 @@ struct AttnArgs {
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
-  float* part_o;    // [max_splits, B*N*Hq, D] fp32, normalised partial outputs
+  __nv_bfloat16* part_o;  // [max_splits, B*N*Hq, D] bf16, normalised partial outputs
   float* part_lse;  // [max_splits, B*N*Hq] fp32, base-2 log-sum-exp of each partial
   int B, N, Hq, Hkv, G, D, W;
   int bs, num_blocks, max_blocks;
   float scale_log2;  // softmax scale * log2(e)
   int chunk_tiles;   // prefix tiles per split
-  int max_splits;
+  int max_splits;    // splits of the longest sequence, the tree's own split included
+  int tree_split;    // 1: the tree block is a split of its own
   int row_tiles;     // ceil(N*G / ROW_TILE)
 };
 
 struct AttnPlan {
   int chunk_tiles;
   int max_splits;
+  int tree_split;
   int row_tiles;
   size_t part_o_bytes;
   size_t part_lse_bytes;

@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for the Blackwell (sm_100 family, here sm_103a)
-// features the attention kernel uses: mbarriers, TMA tensor loads, tensor
+// features the attention kernel uses: mbarriers, TMA tensor loads and stores, tensor
 // memory (TMEM) allocation, tcgen05 MMAs with their commit, TMEM loads and
 // stores, and the shared-memory / instruction descriptors of tcgen05.mma.
 //
@@ -106,6 +106,51 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, uin
       "%6}], [%7];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Tensor stores shared -> global (bulk-group completion).  The box's source
+// in shared memory must have been written by this CTA's threads, each of
+// which then executed fence_proxy_async() before a barrier the issuing thread
+// also passed.  Elements outside the tensor's bounds are not written.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* src, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(src))
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* m, const void* src, int c0, int c1, int c2, int c3,
+                                             int c4) {
+  asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(src))
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Returns once every bulk store this thread committed has finished reading
+// its shared-memory source, so the CTA may reuse that memory or exit; the
+// global writes complete before the grid does.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Named barrier `id` over `count` threads (whole warps) that also returns
+// whether `pred` held on every one of them.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p, q;\n"
+      "  setp.ne.u32 p, %1, 0;\n"
+      "  barrier.cta.red.and.pred q, %2, %3, p;\n"
+      "  selp.u32 %0, 1, 0, q;\n"
+      "}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------- TMEM
