@@ -200,8 +200,8 @@ TS_API ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t 
                         ts_stream stream);
 
 /*
- * Bytes of device workspace tree_verify_greedy needs (per-row partial argmax
- * results and arrival counters).  Host-only.
+ * Bytes of device workspace tree_verify_greedy needs (a packed argmax key per
+ * node and an arrival counter per sequence).  Host-only.
  */
 TS_API size_t tree_verify_workspace_size(int B, int N, int V);
 
@@ -410,18 +410,17 @@ TS_API ts_status tree_verify_greedy_forest(const int32_t* draft_tokens, const fl
  * TS_VERIFY_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library; every GPU that
  * loads the library holds it until the process exits.  Sizes whose scratch
  * (tree_verify_workspace_size(B, N, V)) exceeds that limit return
- * TS_ERR_WORKSPACE before anything is launched.  The need is about
- * 8 * B*N * ceil(V / 8192) + 4 * (B*N + B) bytes: 0.5 MiB for B*N = 4096
- * nodes over a 128256-token vocabulary, so the limit is B*N of about 30000
- * nodes at that vocabulary.
+ * TS_ERR_WORKSPACE before anything is launched.  The need is 8 bytes a
+ * node and 4 a sequence (each part rounded up to 256 bytes), whatever the
+ * vocabulary: 32 KiB for B*N = 4096 nodes, so the limit is B*N of about
+ * 520000 nodes.
  *
  * - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  * - The first call on a device looks up the array's device address (with the
  *   device that owns `stream` current) and caches it; make that first call
  *   before any stream capture.
- * - Each call clears the scratch's arrival counters on `stream` (an async
- *   memset) before its kernel; the array keeps the rest of the previous
- *   call's contents.
+ * - Each call clears the part of the scratch it uses on `stream` (an async
+ *   memset) before its kernel.
  * - Every call on a device shares the one array: calls that can overlap on
  *   the GPU (different streams without ordering between them) race and give
  *   wrong results.  Order them on one stream.

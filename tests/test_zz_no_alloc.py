@@ -70,7 +70,7 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
 def test_noalloc_rejects_problems_beyond_its_scratch():
     ts = _lib()
     a = ctypes.c_void_p(0x10000)
-    B, N, V = 128, 256, 128256       # needs about 4.1 MiB of scratch
+    B, N, V = 2100, 256, 128256      # needs about 4.1 MiB of scratch (8 bytes a node)
     assert ts.tree_verify_workspace_size(B, N, V) > ts.NOALLOC_SCRATCH_BYTES
     st = ts.lib().tree_verify_greedy_noalloc(a, a, a, B, N, V, 8, a, a, a, a, a, None)
     assert st == -8     # TS_ERR_WORKSPACE, returned before anything is launched

@@ -131,19 +131,16 @@ cudaError_t prepare_device(int* stoch_max_cluster = nullptr) {
 
 struct VerifyPlan {
   int chunks;
-  size_t part_v, part_i, row_ticket, seq_ticket, total;
+  size_t row_key, seq_ticket, total;
 };
 
 VerifyPlan plan_verify(int B, int N, int V) {
   VerifyPlan pl{};
   pl.chunks = ceil_div(V, VERIFY_CHUNK);
-  const size_t parts = (size_t)B * N * pl.chunks;
-  // tickets first: they must start zeroed and stay zeroed between calls
-  pl.row_ticket = 0;
-  pl.seq_ticket = round256((size_t)B * N * sizeof(unsigned));
-  pl.part_v = pl.seq_ticket + round256((size_t)B * sizeof(unsigned));
-  pl.part_i = pl.part_v + round256(parts * sizeof(float));
-  pl.total = pl.part_i + round256(parts * sizeof(int32_t));
+  // every byte must start zeroed and is left zeroed by each call
+  pl.row_key = 0;
+  pl.seq_ticket = round256((size_t)B * N * sizeof(unsigned long long));
+  pl.total = pl.seq_ticket + round256((size_t)B * sizeof(unsigned));
   return pl;
 }
 
@@ -166,10 +163,8 @@ ts_status verify_greedy_impl(const int32_t* draft_tokens, const float* target_lo
   a.B = B; a.N = N; a.V = V; a.max_depth = max_depth; a.chunks = pl.chunks;
   a.accepted = accepted; a.accept_len = accept_len; a.bonus = bonus; a.argmax = argmax_out;
   a.status = status;
-  a.row_ticket = reinterpret_cast<unsigned*>(ws + pl.row_ticket);
+  a.row_key = reinterpret_cast<unsigned long long*>(ws + pl.row_key);
   a.seq_ticket = reinterpret_cast<unsigned*>(ws + pl.seq_ticket);
-  a.part_v = reinterpret_cast<float*>(ws + pl.part_v);
-  a.part_i = reinterpret_cast<int32_t*>(ws + pl.part_i);
   a.forest = forest;
   return launch_verify(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
@@ -391,9 +386,9 @@ ts_status tree_verify_greedy_noalloc(const int32_t* draft_tokens, const float* t
   const ts_status st = verify_static_scratch(&scratch, &scratch_bytes);
   if (st != TS_OK) return st;
   if (pl.total > scratch_bytes) return TS_ERR_WORKSPACE;
-  // The array keeps whatever the previous call left; the arrival counters
-  // must start at zero, so clear them on the caller's stream.
-  if (cudaMemsetAsync(scratch, 0, pl.part_v, (cudaStream_t)stream) != cudaSuccess) return TS_ERR_CUDA;
+  // The array keeps whatever the previous call left; the argmax keys and
+  // arrival counters must start at zero, so clear them on the caller's stream.
+  if (cudaMemsetAsync(scratch, 0, pl.total, (cudaStream_t)stream) != cudaSuccess) return TS_ERR_CUDA;
   char* ws = static_cast<char*>(scratch);
   VerifyArgs a{};
   a.draft = draft_tokens;
@@ -402,10 +397,8 @@ ts_status tree_verify_greedy_noalloc(const int32_t* draft_tokens, const float* t
   a.B = B; a.N = N; a.V = V; a.max_depth = max_depth; a.chunks = pl.chunks;
   a.accepted = accepted; a.accept_len = accept_len; a.bonus = bonus; a.argmax = argmax_out;
   a.status = status;
-  a.row_ticket = reinterpret_cast<unsigned*>(ws + pl.row_ticket);
+  a.row_key = reinterpret_cast<unsigned long long*>(ws + pl.row_key);
   a.seq_ticket = reinterpret_cast<unsigned*>(ws + pl.seq_ticket);
-  a.part_v = reinterpret_cast<float*>(ws + pl.part_v);
-  a.part_i = reinterpret_cast<int32_t*>(ws + pl.part_i);
   return launch_verify(a, (cudaStream_t)stream) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 

@@ -123,10 +123,8 @@ struct VerifyArgs {
   int32_t* bonus;
   int32_t* argmax;
   int32_t* status;
-  float* part_v;
-  int32_t* part_i;
-  unsigned* row_ticket;
-  unsigned* seq_ticket;
+  unsigned long long* row_key;  // [B*N] packed (value, index) argmax keys, 0 between calls
+  unsigned* seq_ticket;         // [B] arrival counters, 0 between calls
   int forest;  // several roots allowed; chains stop at -1
 };
 constexpr int VERIFY_THREADS = 256;

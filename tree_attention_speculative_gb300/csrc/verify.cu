@@ -12,11 +12,15 @@
 // VERIFY_CHUNK floats, one CTA per (row, chunk).  Each CTA streams its chunk
 // with 16-byte loads (all of a thread's loads are issued before any is used),
 // keeps a running (max, first index) per thread, and reduces it with warp
-// shuffles and one shared-memory step.  The last CTA to finish a row (an
-// atomicInc ticket that wraps back to 0) folds the row's chunk partials; the
-// last row to finish a sequence (a second wrapping ticket) runs the acceptance
-// walk for that sequence, one thread per node.  No CTA ever waits for another,
-// so nothing here can hang; the tickets return to zero by themselves.
+// shuffles and one shared-memory step.  The CTA's result is folded into the
+// row's 64-bit key with one atomicMax: the high word is the value mapped to
+// an order-preserving unsigned, the low word 0xFFFFFFFF - index, so the
+// larger value and, on ties, the smaller index win, and every real key is
+// above 0.  The last CTA to finish a sequence (an atomicInc ticket that
+// wraps back to 0) decodes the row keys into argmax, sets them back to 0 and
+// runs the acceptance walk, one thread per node.  No CTA ever waits for
+// another, so nothing here can hang; the keys and tickets return to zero by
+// themselves.
 #include <cfloat>
 #include <climits>
 #include <mutex>
@@ -31,6 +35,14 @@ __device__ __forceinline__ void take_better(float& v, int& i, float v2, int i2) 
     v = v2;
     i = i2;
   }
+}
+
+// Order-preserving map of a finite float to an unsigned (larger float, larger
+// unsigned); -inf maps to 0x007FFFFF, so the packed key of any value is > 0.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int i) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (0xFFFFFFFFu - (uint32_t)i);
 }
 
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
@@ -71,6 +83,9 @@ k_verify(VerifyArgs a) {
   const int lo = chunk * VERIFY_CHUNK;
   const int hi = min(a.V, lo + VERIFY_CHUNK);
 
+  // Each thread starts at (-inf, its first index), so a row of nothing but
+  // -inf still yields its first index; a thread with no element keeps
+  // INT_MAX, which loses every tie.
   float bv = -INFINITY;
   int bi = INT_MAX;
   const bool vec = ((reinterpret_cast<uintptr_t>(x + lo) & 15) == 0) && (((hi - lo) & 3) == 0);
@@ -78,6 +93,7 @@ k_verify(VerifyArgs a) {
     constexpr int PER = VERIFY_CHUNK / (4 * VERIFY_THREADS);  // float4 per thread in a full chunk
     const float4* x4 = reinterpret_cast<const float4*>(x + lo);
     const int n4 = (hi - lo) >> 2;
+    if ((int)threadIdx.x < n4) bi = lo + 4 * threadIdx.x;
     float4 r[PER];
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
@@ -94,45 +110,20 @@ k_verify(VerifyArgs a) {
       if (r[k].w > bv) { bv = r[k].w; bi = base + 3; }
     }
   } else {
+    if (lo + (int)threadIdx.x < hi) bi = lo + threadIdx.x;
     for (int e = lo + threadIdx.x; e < hi; e += VERIFY_THREADS) {
       const float v = x[e];
       if (v > bv) { bv = v; bi = e; }
     }
   }
-  // A thread that saw only -inf (or nothing) must not claim an index ahead of
-  // one that saw a real -inf at a smaller index: its INT_MAX sentinel loses ties.
   block_argmax(bv, bi);
 
   __shared__ int s_flag;
-  if (a.chunks > 1) {
-    if (threadIdx.x == 0) {
-      a.part_v[blockIdx.x] = bv;
-      a.part_i[blockIdx.x] = bi;
-      __threadfence();
-      const unsigned old = atomicInc(&a.row_ticket[row], (unsigned)(a.chunks - 1));
-      s_flag = (old == (unsigned)(a.chunks - 1));
-    }
-    __syncthreads();
-    if (!s_flag) return;
-    __threadfence();
-    // last chunk of this row: fold the row's partials (chunks <= 32 per row is
-    // not assumed; a strided loop covers any count)
-    float v = -INFINITY;
-    int i = INT_MAX;
-    for (int c = threadIdx.x; c < a.chunks; c += VERIFY_THREADS) {
-      take_better(v, i, __ldcg(a.part_v + (size_t)row * a.chunks + c),
-                  __ldcg(a.part_i + (size_t)row * a.chunks + c));
-    }
-    __syncthreads();
-    block_argmax(v, i);
-    bv = v;
-    bi = i;
-  }
   if (threadIdx.x == 0) {
-    a.argmax[row] = bi;
+    atomicMax(&a.row_key[row], argmax_key(bv, bi));
     __threadfence();
-    const unsigned old = atomicInc(&a.seq_ticket[b], (unsigned)(a.N - 1));
-    s_flag = (old == (unsigned)(a.N - 1));
+    const unsigned last = (unsigned)(a.N * a.chunks - 1);
+    s_flag = (atomicInc(&a.seq_ticket[b], last) == last);
   }
   __syncthreads();
   if (!s_flag) return;
@@ -149,7 +140,11 @@ k_verify(VerifyArgs a) {
     ok = (t == 0) ? (p == -1) : ((p >= 0 && p < t) || (a.forest && p == -1));
     s_par[t] = p;
     s_draft[t] = a.draft[(size_t)b * N + t];
-    s_pred[t] = __ldcg(a.argmax + (size_t)b * N + t);
+    unsigned long long* key = a.row_key + (size_t)b * N + t;
+    const int am = (int)(0xFFFFFFFFu - (uint32_t)(__ldcg(key) & 0xFFFFFFFFull));
+    *key = 0ull;  // ready for the next call
+    s_pred[t] = am;
+    a.argmax[(size_t)b * N + t] = am;
   }
   const int valid = __syncthreads_and(ok);
   int32_t* acc_row = a.accepted + (size_t)b * (a.max_depth + 1);
