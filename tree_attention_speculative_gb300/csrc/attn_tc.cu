@@ -140,6 +140,13 @@ __device__ __forceinline__ bool wait_count(const int* counter, int target, volat
   }
 }
 
+// A plain global load the compiler may not move: issued where it is written.
+__device__ __forceinline__ int ld_global_early(const int* p) {
+  int v;
+  asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(reinterpret_cast<uint64_t>(p)) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -161,6 +168,29 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rt = blockIdx.x, split = blockIdx.y, unit = blockIdx.z;
   const int b = unit / a.Hkv, g = unit - b * a.Hkv;
+  const int t_begin = split * a.chunk_tiles;
+  const int boxes = KV_TILE / args.box_rows;  // boxes (paged blocks) per tile (1 .. 8)
+  const int tpg = 32 / boxes;                 // tiles per group of block-table entries
+  const int* table_row = a.block_table + (size_t)b * a.max_blocks;
+  // First of all, by a warp that has no part in the set-up: fetch the tensor
+  // maps (kernel parameters) and prefetch into L2 the Q tile and the
+  // block-table entry of this split's first tile, so that their address
+  // translation and DRAM latency overlap the set-up and the wait (prefetches
+  // read no data; see sm100.cuh).
+  if (warp == V_PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_vc);
+    tma_prefetch_desc(&tm_kt);
+    tma_prefetch_desc(&tm_vt);
+    for (int hh = 0; hh < C::HALVES; ++hh) tma_prefetch_4d(&tm_q, 64 * hh, g * a.G, rt * (ROW_TILE / a.G), b);
+    if (a.max_blocks > 0) {
+      // the 16-byte piece holding the entry, through the bulk-copy unit
+      const long long idx = (long long)t_begin * KV_TILE / a.bs;
+      const uintptr_t e = reinterpret_cast<uintptr_t>(table_row + (idx < a.max_blocks ? idx : a.max_blocks - 1));
+      bulk_prefetch_l2(reinterpret_cast<const void*>(e & ~uintptr_t(15)), 16);
+    }
+  }
 
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
@@ -186,33 +216,26 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  // the tensor maps are kernel parameters: fetch them before the wait
-  if (warp == PRODUCER_WARP && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_kc);
-    tma_prefetch_desc(&tm_vc);
-    tma_prefetch_desc(&tm_kt);
-    tma_prefetch_desc(&tm_vt);
-  }
   // everything above touched no global memory and overlaps the previous
   // kernel's tail; wait for it before reading any input.  The next kernel is
   // released only at this CTA's teardown (released at the start, its CTAs
   // were measured to delay this kernel's first loads by about 2 us).
   pdl_wait();
-  const int t_begin = split * a.chunk_tiles;
-  const int boxes = KV_TILE / args.box_rows;  // boxes (paged blocks) per tile (1 .. 8)
-  const int tpg = 32 / boxes;                 // tiles per group of block-table entries
-  const int* table_row = a.block_table + (size_t)b * a.max_blocks;
-  const int p_dev = a.prefix_len[b];
-  // The producers fetch their first group of block-table entries before the
-  // prefix length is known (index clamped to the table's row), so that the
-  // two loads overlap; entries past the prefix are discarded below.
+  // The producers fetch their first group of block-table entries together
+  // with the prefix length (index clamped to the table's row; entries past
+  // the prefix are discarded below).  Volatile loads, so that the compiler
+  // keeps the table load here instead of sinking it behind the branch on the
+  // prefix length, which would serialise the two latencies.
   int blk_first = 0;
-  if ((warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && a.max_blocks > 0) {
+  const bool producer = (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && a.max_blocks > 0;
+  const int* blk_addr = table_row;
+  if (producer) {
     const long long t0 = (long long)(t_begin + lane / boxes) * KV_TILE + (lane % boxes) * args.box_rows;
     const long long idx = t0 / a.bs;
-    blk_first = table_row[idx < a.max_blocks ? idx : a.max_blocks - 1];
+    blk_addr = table_row + (idx < a.max_blocks ? idx : a.max_blocks - 1);
   }
+  const int p_dev = ld_global_early(a.prefix_len + b);
+  if (producer) blk_first = ld_global_early(blk_addr);
   int P;
   const bool p_ok = usable_prefix(p_dev, a.chunk_tiles, a.max_splits, a.tree_split, a.bs, a.max_blocks, &P);
   const int tiles = prefix_tiles(P);

@@ -108,6 +108,28 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// L2 prefetches.  They return no data and change no value anyone reads (L2
+// is the device's point of coherence), so a kernel may issue them before its
+// programmatic-dependent-launch wait, on inputs the previous kernel may still
+// be writing: the address translation and the DRAM fetch then overlap that
+// wait.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
+// bytes: a multiple of 16; p: 16-byte aligned.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* m, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
 // Tensor stores shared -> global (bulk-group completion).  The box's source
 // in shared memory must have been written by this CTA's threads, each of
 // which then executed fence_proxy_async() before a barrier the issuing thread

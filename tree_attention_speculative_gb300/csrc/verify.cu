@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "internal.cuh"
+#include "sm100.cuh"
 
 namespace ts {
 
@@ -72,16 +73,22 @@ __device__ __forceinline__ void block_argmax(float& v, int& i) {
   }
 }
 
-__global__ void __launch_bounds__(VERIFY_THREADS)
+// Eight CTAs per SM (32 registers a thread), so a grid of up to 8 * SMs CTAs
+// is resident at once.
+__global__ void __launch_bounds__(VERIFY_THREADS, 8)
 k_verify(VerifyArgs a) {
-  pdl_wait();
-  pdl_trigger();
   const int row = blockIdx.x / a.chunks;
   const int chunk = blockIdx.x - row * a.chunks;
   const int b = row / a.N;
   const float* x = a.logits + (size_t)row * a.V;
   const int lo = chunk * VERIFY_CHUNK;
   const int hi = min(a.V, lo + VERIFY_CHUNK);
+  // Prefetch this chunk into L2 while the previous kernel finishes (a
+  // prefetch reads no data, so it may precede the wait; see sm100.cuh).
+  if (threadIdx.x == 0 && ((reinterpret_cast<uintptr_t>(x + lo) & 15) == 0) && hi - lo >= 4)
+    sm100::bulk_prefetch_l2(x + lo, (uint32_t)((hi - lo) * 4) & ~15u);
+  pdl_wait();
+  pdl_trigger();
 
   // Each thread starts at (-inf, its first index), so a row of nothing but
   // -inf still yields its first index; a thread with no element keeps
