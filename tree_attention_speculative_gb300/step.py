@@ -4,7 +4,8 @@
 which is only the allocator here) for fixed sizes and enqueues
 tree_build_ancestry -> tree_attn_fwd -> tree_verify_greedy on one stream (their
 _forest variants with ``forest=True``).  Every computation happens in the
-library's kernels.
+library's kernels.  ``PackedInputs`` stages a step's inputs from host memory
+in one copy.
 """
 from __future__ import annotations
 
@@ -16,6 +17,50 @@ import torch
 from . import (attn_params, tree_attn_fwd, tree_attn_workspace_size, tree_build_ancestry,
                tree_build_ancestry_forest, tree_verify_greedy, tree_verify_greedy_forest,
                tree_verify_workspace_size)
+
+
+class PackedInputs:
+    """A step's inputs packed into one pinned host buffer and one device buffer
+    (every tensor at a 256-byte aligned offset), so that the whole host-to-device
+    upload of a step is a single copy, which can run on a stream of its own
+    while the previous step computes.
+
+    ``arrays`` maps names to CPU tensors (any dtype); ``device(name)`` is the
+    device view to hand to the library's calls, ``upload(stream)`` enqueues the
+    copy.  Torch is only the allocator and the copy call here.
+    """
+
+    ALIGN = 256
+
+    def __init__(self, arrays: dict, device):
+        self.layout = {}
+        off = 0
+        for name, t in arrays.items():
+            t = t.contiguous()
+            self.layout[name] = (off, tuple(t.shape), t.dtype)
+            off += -(-(t.numel() * t.element_size()) // self.ALIGN) * self.ALIGN
+        self.nbytes = off
+        self.host = torch.empty(off, dtype=torch.uint8)
+        if torch.device(device).type == "cuda":
+            self.host = self.host.pin_memory()
+        self.dev = torch.empty(off, dtype=torch.uint8, device=device)
+        for name, t in arrays.items():
+            self.host_view(name).copy_(t)
+
+    def _view(self, buf: torch.Tensor, name: str) -> torch.Tensor:
+        off, shape, dtype = self.layout[name]
+        n = int(np.prod(shape, dtype=np.int64)) * torch.empty((), dtype=dtype).element_size()
+        return buf[off:off + n].view(dtype).view(shape)
+
+    def host_view(self, name: str) -> torch.Tensor:
+        return self._view(self.host, name)
+
+    def device(self, name: str) -> torch.Tensor:
+        return self._view(self.dev, name)
+
+    def upload(self, stream=None) -> None:
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream(self.dev.device)):
+            self.dev.copy_(self.host, non_blocking=True)
 
 
 class TreeVerifyStep:
