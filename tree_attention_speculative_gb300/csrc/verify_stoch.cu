@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(STOCH_THREADS, 2) k_verify_stoch(StochArgs a) 
 
   issue(0, N > 1);
 
-  // tree and draft tokens; every CTA checks them and reaches the same verdict
+  // tree and draft tokens; every CTA checks them and reaches the same conclusion
   bool bad = false;
   for (int i = tid; i < N; i += STOCH_THREADS) {
     const int p = a.parent[(size_t)b * N + i];
