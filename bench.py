@@ -28,6 +28,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -97,15 +98,24 @@ def recorded_traffic(kernel: str, workload: str):
             k, v = line.split(":", 1)
             rec[k.strip()] = v.strip()
     try:
-        srcs = rec["sources"].split()
-        h = hashlib.sha256()
-        for s in srcs:
-            h.update(open(os.path.join(ROOT, s), "rb").read())
-        if h.hexdigest()[:16] != rec["sources_sha256_16"]:
+        if code_digest(rec["sources"].split()) != rec["sources_sha256_16"]:
             return None
         return int(float(rec["dram_bytes_per_launch"]))
     except Exception:
         return None
+
+
+def code_digest(sources) -> str:
+    """First 16 hex digits of the sha256 of the sources' code: '//' comments,
+    trailing blanks and empty lines removed, so that editing a comment does not
+    disown a capture of an unchanged kernel."""
+    h = hashlib.sha256()
+    for s in sources:
+        for line in open(os.path.join(ROOT, s), encoding="utf-8"):
+            code = re.sub(r"//.*$", "", line).rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
 
 
 # ----------------------------------------------------------------------------- clocks

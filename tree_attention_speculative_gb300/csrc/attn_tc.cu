@@ -21,7 +21,9 @@
 //              stores the boxes: the output itself, or this split's partial.
 //   warp 4     TMEM allocation; TMA loads of the Q tile and of the K tiles
 //   warp 7     TMA loads of the V tiles (paged blocks: one box per block); K
-//              and V each stream through their own 3-stage ring.
+//              and V each stream through their own 3-stage ring.  At CTA
+//              start it also prefetches the tensor maps, the Q tile and the
+//              first block-table entry into L2, ahead of the launch wait.
 //   warp 5     QK issuer (one thread): S(j) = Q K(j)^T, both operands in
 //              swizzled shared memory, into S buffer j%3 once PV(j-3) (the
 //              last reader of that buffer) has completed (s_free[j%3]).
