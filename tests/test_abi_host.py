@@ -88,6 +88,41 @@ def test_attn_plan_query(ts):
     assert ts.lib().tree_attn_plan(ctypes.byref(bad), None, None, None) == -4
 
 
+@pytest.mark.parametrize("B,N,Hq,Hkv,D,bs,P", [
+    (1, 64, 32, 8, 128, 4096, (4096,)),                  # c2-shaped: one wave, tree on its own split
+    (16, 26, 32, 8, 128, 16, tuple(range(1024, 16385, 1024))),
+    (64, 64, 64, 8, 128, 16, (8192,) * 64),              # many waves: one split per unit
+    (4, 192, 32, 8, 128, 64, (131072,) * 4),
+    (3, 5, 2, 2, 64, 16, (0, 0, 0)),                     # no prefix at all
+    (2, 256, 1, 1, 64, 16, (0, 5000)),
+])
+def test_attn_plan_covers_the_prefix_and_sizes_the_workspace(ts, B, N, Hq, Hkv, D, bs, P):
+    p = _params(ts, B=B, N=N, Hq=Hq, Hkv=Hkv, D=D, bs=bs, P=P)
+    plan = ts.tree_attn_plan(p)
+    chunk, splits, tsplit = plan["chunk_tiles"], plan["max_splits"], plan["tree_split"]
+    tiles = max(-(-x // 128) for x in P)
+    # the prefix splits of the longest sequence hold all its tiles, and no split is empty
+    assert chunk * (splits - tsplit) >= tiles
+    if tiles:
+        assert chunk * (splits - tsplit - 1) < tiles
+    else:
+        assert splits == 1
+    rows = B * N * Hq
+    ws = ts.tree_attn_workspace_size(p)
+    if splits == 1:
+        assert ws == 256
+    else:
+        r256 = lambda x: -(-x // 256) * 256
+        assert ws == r256(splits * rows * D * 2) + r256(splits * rows * 4)
+
+
+def test_attn_plan_gives_the_tree_its_own_split_on_one_wave(ts):
+    plan = ts.tree_attn_plan(_params(ts, B=1, N=64, Hq=32, Hkv=8, D=128, bs=4096, P=(4096,)))
+    assert plan == {"chunk_tiles": 4, "max_splits": 9, "tree_split": 1}
+    plan = ts.tree_attn_plan(_params(ts, B=64, N=64, Hq=64, Hkv=8, D=128, bs=16, P=(8192,) * 64))
+    assert plan["max_splits"] == 1 and plan["tree_split"] == 0
+
+
 def _plan_of(ts, name, B, N, Hq, Hkv, D, plens, bs, tree):
     return ts.tree_attn_plan(_params(ts, B=B, N=N, Hq=Hq, Hkv=Hkv, D=D, bs=bs, P=tuple(plens)))
 
