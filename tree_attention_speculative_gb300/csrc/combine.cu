@@ -9,7 +9,9 @@
 // D/8 lanes per output row (b, node, head): each lane owns 8 consecutive
 // channels, so every partial read and the output store is one 16-byte access
 // per lane and a warp merges 32/(D/8) rows at once.  The splits are taken in
-// groups of eight: a group's lse and O loads are all in flight at once (the
+// groups of GRP (8, or 16 when a sequence may have more than 8 splits, so
+// that up to 16 take one round trip): a group's lse and O loads are all in
+// flight at once (the
 // first group's are issued together with the prefix-length load, for every
 // split the workspace holds, and the ones past this sequence's split count
 // are dropped), and a running maximum rescales the sums between groups.
@@ -19,7 +21,6 @@
 namespace ts {
 
 constexpr int COMBINE_THREADS = 128;
-constexpr int COMBINE_GROUP = 8;
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -31,7 +32,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
   }
 }
 
-template <int D>
+template <int D, int GRP>
 __global__ void __launch_bounds__(COMBINE_THREADS)
 k_combine(AttnArgs a) {
   constexpr int LPR = D / 8;                        // lanes per row
@@ -46,11 +47,11 @@ k_combine(AttnArgs a) {
   const size_t stride_lse = (size_t)rows;
   const size_t stride_o = (size_t)rows * D;
 
-  float w[COMBINE_GROUP];
-  uint4 raw[COMBINE_GROUP];
+  float w[GRP];
+  uint4 raw[GRP];
   auto load_group = [&](int s0, int limit) {
 #pragma unroll
-    for (int i = 0; i < COMBINE_GROUP; ++i) {
+    for (int i = 0; i < GRP; ++i) {
       const int s = s0 + i;
       w[i] = -INFINITY;
       raw[i] = make_uint4(0, 0, 0, 0);
@@ -70,11 +71,11 @@ k_combine(AttnArgs a) {
   float acc[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-  for (int s0 = 0; s0 < ns; s0 += COMBINE_GROUP) {
+  for (int s0 = 0; s0 < ns; s0 += GRP) {
     if (s0 > 0) load_group(s0, ns);
     float gm = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < COMBINE_GROUP; ++i)
+    for (int i = 0; i < GRP; ++i)
       if (s0 + i < ns) gm = fmaxf(gm, w[i]);
     const float m_new = fmaxf(m, gm);
     const float f = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
@@ -83,7 +84,7 @@ k_combine(AttnArgs a) {
     for (int k = 0; k < 8; ++k) acc[k] *= f;
     m = m_new;
 #pragma unroll
-    for (int i = 0; i < COMBINE_GROUP; ++i) {
+    for (int i = 0; i < GRP; ++i) {
       if (s0 + i < ns) {
         const float wi = exp2f(w[i] - m);
         den += wi;
@@ -110,8 +111,12 @@ cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s) {
   const int rows = a.B * a.N * a.Hq;
   const int per_block = COMBINE_THREADS / (a.D / 8);
   const int grid = ceil_div(rows, per_block);
-  return a.D == 128 ? launch_pdl(k_combine<128>, dim3(grid), dim3(COMBINE_THREADS), 0, s, a)
-                   : launch_pdl(k_combine<64>, dim3(grid), dim3(COMBINE_THREADS), 0, s, a);
+  const bool wide = a.max_splits > 8;
+  if (a.D == 128)
+    return wide ? launch_pdl(k_combine<128, 16>, dim3(grid), dim3(COMBINE_THREADS), 0, s, a)
+                : launch_pdl(k_combine<128, 8>, dim3(grid), dim3(COMBINE_THREADS), 0, s, a);
+  return wide ? launch_pdl(k_combine<64, 16>, dim3(grid), dim3(COMBINE_THREADS), 0, s, a)
+              : launch_pdl(k_combine<64, 8>, dim3(grid), dim3(COMBINE_THREADS), 0, s, a);
 }
 
 }  // namespace ts

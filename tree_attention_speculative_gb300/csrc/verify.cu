@@ -87,6 +87,12 @@ k_verify(VerifyArgs a) {
   // prefetch reads no data, so it may precede the wait; see sm100.cuh).
   if (threadIdx.x == 0 && ((reinterpret_cast<uintptr_t>(x + lo) & 15) == 0) && hi - lo >= 4)
     sm100::bulk_prefetch_l2(x + lo, (uint32_t)((hi - lo) * 4) & ~15u);
+  // the sequence's draft tokens and parents, which its walk reads (one
+  // 128-byte line per thread, by the sequence's first CTA)
+  if (row == b * a.N && chunk == 0 && (int)threadIdx.x * 32 < a.N) {
+    sm100::prefetch_l2(a.draft + (size_t)b * a.N + threadIdx.x * 32);
+    sm100::prefetch_l2(a.parent + (size_t)b * a.N + threadIdx.x * 32);
+  }
   pdl_wait();
   pdl_trigger();
 
