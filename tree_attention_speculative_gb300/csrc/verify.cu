@@ -134,13 +134,14 @@ k_verify(VerifyArgs a) {
   __shared__ int s_flag;
   if (threadIdx.x == 0) {
     atomicMax(&a.row_key[row], argmax_key(bv, bi));
-    __threadfence();
+    __threadfence();  // the key before the ticket
     const unsigned last = (unsigned)(a.N * a.chunks - 1);
-    s_flag = (atomicInc(&a.seq_ticket[b], last) == last);
+    const bool is_last = atomicInc(&a.seq_ticket[b], last) == last;
+    if (is_last) __threadfence();  // every other CTA's key before this CTA's reads (the barrier passes it on)
+    s_flag = is_last;
   }
   __syncthreads();
   if (!s_flag) return;
-  __threadfence();
 
   // ---- acceptance walk for sequence b (this CTA saw every row of b finish) ----
   __shared__ int s_par[MAX_NODES], s_draft[MAX_NODES], s_pred[MAX_NODES];
