@@ -11,11 +11,11 @@
 // per lane and a warp merges 32/(D/8) rows at once.  The splits are taken in
 // groups of GRP (8, or 16 when a sequence may have more than 8 splits, so
 // that up to 16 take one round trip): a group's lse and O loads are all in
-// flight at once (the
-// first group's are issued together with the prefix-length load, for every
-// split the workspace holds, and the ones past this sequence's split count
-// are dropped), and a running maximum rescales the sums between groups.
-// 128-thread blocks so that a block fits beside an attention CTA.
+// flight at once (the first group's are issued together with the
+// prefix-length load, for every split the workspace holds, and the ones past
+// this sequence's split count are dropped), and a running maximum rescales
+// the sums between groups.  128-thread blocks; the 8-wide kernel (71
+// registers) fits beside an attention CTA on one SM.
 #include "internal.cuh"
 
 namespace ts {
