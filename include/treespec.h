@@ -122,9 +122,11 @@ TS_API ts_status tree_build_ancestry(const int32_t* parent_idx, const int32_t* p
  *               A contiguous cache is the special case block_size = P,
  *               block_table[b] = {b}.
  *   block_table [B, max_blocks] int32; only the first ceil(P_b / block_size)
- *               entries of row b are read.
+ *               entries of row b are used (other entries of the row may be
+ *               read, never followed).
  *   prefix_len  [B] int32 device copy of P_b; prefix_len_host the same values
  *               in host memory (used to plan the split of the prefix).
+ *               0 <= P_b <= 2^30.
  *   k_tree,
  *   v_tree      [B, N, Hkv, D] bf16, keys/values of the tree nodes themselves.
  *   anc_mask    [B, N, W] uint64 from tree_build_ancestry.
@@ -255,7 +257,8 @@ TS_API ts_status tree_verify_greedy(const int32_t* draft_tokens, const float* ta
  *                    tree_attn_fwd).
  *   accepted         [B, max_depth + 1] int32 and accept_len [B] int32 from
  *                    tree_verify_greedy.
- *   prefix_len       [B] int32, P_b before the commit.
+ *   prefix_len       [B] int32, P_b before the commit; a sequence with P_b
+ *                    outside [0, 2^30] commits nothing and keeps it.
  *   k_cache, v_cache [num_blocks, Hkv, block_size, D] bf16, written at rows
  *                    (t mod block_size) of blocks block_table[b, t div
  *                    block_size] for t = P_b .. P_b + L; nothing else changes.

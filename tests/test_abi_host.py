@@ -150,6 +150,7 @@ def test_small_parity_cases_cover_every_split_layout(ts):
     (dict(rope_theta=10000.0), -4),
     (dict(misalign=True), -2),
     (dict(neg_prefix=True), -2),
+    (dict(huge_prefix=True), -4),
 ])
 def test_attn_rejects_before_launch(ts, change, code):
     change = dict(change)
@@ -158,6 +159,8 @@ def test_attn_rejects_before_launch(ts, change, code):
         p.q = 0x10002
     elif change.pop("neg_prefix", False):
         p = _params(ts, P=(5, -1))
+    elif change.pop("huge_prefix", False):
+        p = _params(ts, P=(5, (1 << 30) + 16))
     elif "q" in change:
         p = _params(ts)
         p.q = None

@@ -34,6 +34,7 @@ ts_status check_attn(const ts_attn_params* p) {
   for (int b = 0; b < p->B; ++b) {
     const int P = p->prefix_len_host[b];
     if (P < 0) return TS_ERR_SHAPE;
+    if (P > (1 << 30)) return TS_ERR_UNSUPPORTED;  // keeps every token index in 32-bit arithmetic
     if (ceil_div(P, bs) > p->max_blocks) return TS_ERR_SHAPE;
   }
   if (!aligned16(p->q) || !aligned16(p->k_cache) || !aligned16(p->v_cache) || !aligned16(p->k_tree) ||

@@ -28,7 +28,8 @@ k_commit(CommitArgs a) {
   const int st = a.status ? a.status[b] : TS_OK;
   const int L = a.accept_len[b];
   const int vec = a.D / 8;  // uint4 per key row
-  const bool commit = (st == TS_OK) && L >= 0 && L <= a.max_depth && P >= 0;
+  // P bounded so that every position P + d stays far inside int range
+  const bool commit = (st == TS_OK) && L >= 0 && L <= a.max_depth && P >= 0 && P <= (1 << 30);
   const int n = commit ? (L + 1) * a.Hkv * vec : 0;
 
   // validate every destination before writing any
@@ -38,7 +39,7 @@ k_commit(CommitArgs a) {
     const int node = a.accepted[(size_t)b * (a.max_depth + 1) + d];
     const int t = P + d;
     const int bi = t / a.bs;
-    const int blk = bi < a.max_blocks ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
+    const int blk = (bi >= 0 && bi < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
     ok = ok && node >= 0 && node < a.N && blk >= 0 && blk < a.num_blocks;
   }
   const int all_ok = __syncthreads_and(ok);
