@@ -218,16 +218,16 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  // everything above touched no global memory and overlaps the previous
-  // kernel's tail; wait for it before reading any input.  The next kernel is
+  // everything above read no global memory (prefetches return no data) and
+  // overlaps the previous kernel's tail; wait for it before reading any
+  // input.  The next kernel is
   // released only at this CTA's teardown (released at the start, its CTAs
   // were measured to delay this kernel's first loads by about 2 us).
   pdl_wait();
   // The producers fetch their first group of block-table entries together
   // with the prefix length (index clamped to the table's row; entries past
-  // the prefix are discarded below).  Volatile loads, so that the compiler
-  // keeps the table load here instead of sinking it behind the branch on the
-  // prefix length, which would serialise the two latencies.
+  // the prefix are discarded below).  Volatile loads: both are issued here,
+  // ahead of the branch on the prefix length, so their latencies overlap.
   int blk_first = 0;
   const bool producer = (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && a.max_blocks > 0;
   const int* blk_addr = table_row;
