@@ -220,7 +220,8 @@ TS_API size_t tree_verify_workspace_size(int B, int N, int V);
  * node (ties: smallest index).
  *
  *   draft_tokens  [B, N] int32 draft token id of each node (the root's is unused).
- *   target_logits [B, N, V] fp32, finite; the argmax takes the first index on ties.
+ *   target_logits [B, N, V] fp32, finite or -inf (a row of nothing but -inf
+ *                 gives index 0); the argmax takes the first index on ties.
  *   parent_idx    [B, N] int32 as for tree_build_ancestry.
  *   accepted      [B, max_depth + 1] int32 out: node ids root .. n*, then -1.
  *   accept_len    [B] int32 out: depth(n*), the number of accepted drafts.
