@@ -84,3 +84,19 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "c1",
                         "--steps", "1"], capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_code_digest_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_text("// header\n__global__ void k(int* x) {\n  x[0] = 1;  // store\n}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d0 = bench.code_digest(["k.cu"])
+    src.write_text("// a different header\n\n__global__ void k(int* x) {\n  x[0] = 1;   // other words\n}\n")
+    assert bench.code_digest(["k.cu"]) == d0
+    src.write_text("// header\n__global__ void k(int* x) {\n  x[0] = 2;  // store\n}\n")
+    assert bench.code_digest(["k.cu"]) != d0
+
+
+
+def test_traffic_record_of_an_unknown_workload_is_none():
+    assert bench.recorded_traffic("tree_attn_fwd", "no-such-workload") is None
