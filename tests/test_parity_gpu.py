@@ -97,6 +97,20 @@ def test_attention_small_elementwise(spec):
     np.testing.assert_allclose(step.lse.cpu().numpy(), ref_lse, rtol=0, atol=LSE_ATOL)
 
 
+@pytest.mark.parametrize("plens", [[896, 300], [1000, 129], [1920, 640], [2000, 0]],
+                         ids=["8-splits", "9-splits", "16-splits", "17-splits"])
+def test_attention_combine_group_boundaries(plens):
+    """Split counts on both sides of the combine's load groups (8 and 16 splits
+    a round trip), with a second, shorter sequence whose rows use fewer splits
+    than the grid holds."""
+    case = _small_case("groups", 2, 33, 4, 1, 128, plens, 64, "levels")
+    step, _ = run_case(case)
+    ref, ref_lse = oracle.attention.tree_attention_case(case)
+    assert step.status.cpu().tolist() == [0, 0]
+    assert_close_attention(out_f64(step), ref, f"splits {plens}")
+    np.testing.assert_allclose(step.lse.cpu().numpy(), ref_lse, rtol=0, atol=LSE_ATOL)
+
+
 def test_attention_hot_keys_softmax_range():
     case = W.build_case("hot", 3, W.tree_random_levels(W.rng(1, "h"), 48, 6), [700, 1500], Hq=8, Hkv=2,
                         D=128, bs=64, permute=True, hot_key_frac=0.05, hot_key_scale=8.0)
