@@ -557,11 +557,9 @@ def run_commit(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     kw = workload_overrides(args)
-    probe = W.make(args.workload, **kw)
-    if not probe.vocab:
+    if args.workload not in W.VOCAB:
         raise SystemExit("--part commit needs a workload with logits (c1, c2, c4, c5)")
-    depth = int(max(oracle.tree.depths(p).max() for p in probe.parent))
-    del probe
+    depth = W.LEVELS[args.workload]
     case = W.make(args.workload, spare_tokens=depth + 1, **kw)
     t = to_dev(case, dev)
     st = TreeVerifyStep(case.B, case.N, case.Hq, case.Hkv, case.D, case.prefix_len, vocab=case.vocab,
@@ -644,7 +642,7 @@ def run_stochastic(args, world, rank, local):
     parent = sets[0][0]
     B, N = parent.shape
     V = sets[0][1].logits.shape[2]
-    depth = int(max(oracle.tree.depths(p).max() for p in parent))
+    depth = W.LEVELS[args.workload]
     dsets = []
     for _, si in sets:
         dsets.append(dict(draft=torch.from_numpy(si.draft).to(dev), logits=torch.from_numpy(si.logits).to(dev),

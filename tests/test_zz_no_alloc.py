@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 
 
@@ -65,6 +66,13 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
             for k in ref:
                 assert torch.equal(got[k], ref[k]), k
         assert ref["accept_len"].cpu().tolist() == case.planted_len.tolist()
+        # and the CPU oracle, which shares no code with either entry point
+        acc, L, bonus, am, st = oracle.verify.verify_greedy(case.draft, case.logits, case.parent, max_depth)
+        np.testing.assert_array_equal(got["accepted"].cpu().numpy(), acc)
+        np.testing.assert_array_equal(got["accept_len"].cpu().numpy(), L)
+        np.testing.assert_array_equal(got["bonus"].cpu().numpy(), bonus)
+        np.testing.assert_array_equal(got["argmax"].cpu().numpy(), am)
+        np.testing.assert_array_equal(got["status"].cpu().numpy(), st)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():

@@ -40,8 +40,11 @@ __device__ __forceinline__ void take_better(float& v, int& i, float v2, int i2) 
 
 // Order-preserving map of a finite float to an unsigned (larger float, larger
 // unsigned); -inf maps to 0x007FFFFF, so the packed key of any value is > 0.
+// -0.0 is first turned into +0.0: the two compare equal, so between chunks,
+// as inside one, a tie at zero must go to the smaller index.
 __device__ __forceinline__ unsigned long long argmax_key(float v, int i) {
-  const uint32_t u = __float_as_uint(v);
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
   const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return ((unsigned long long)ord << 32) | (0xFFFFFFFFu - (uint32_t)i);
 }

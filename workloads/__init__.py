@@ -464,6 +464,9 @@ def workload_trees(name: str, seed: int, batch: int = 64, forest_roots: int = 0)
 
 
 SEEDS = {"c1": 20260001, "c2": 20260002, "c3": 20260003, "c4": 20260004, "c5": 20260005}
+# Deepest level each workload's tree generator draws (every level up to it is
+# populated, so it is also the depth of the deepest node).
+LEVELS = {"c1": 2, "c2": 6, "c3": 5, "c4": 8, "c5": 10}
 VOCAB = {"c1": 1000, "c2": 128256, "c4": 128256, "c5": 128256}
 
 
