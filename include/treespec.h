@@ -202,6 +202,27 @@ TS_API ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t 
                         ts_stream stream);
 
 /*
+ * tree_attn_fwd_stall_test — for testing the failure path only; the pages
+ * have no counterpart.  Runs exactly what tree_attn_fwd runs, except that
+ * every attention CTA of sequence `stall_seq` stops its key stream before its
+ * tile `stall_tile` (128-token tiles, counted from the start of the CTA's
+ * split; the tree block's tiles come last): those loads are never issued, so
+ * the wait for them runs out after `wait_limit_us` microseconds, and every
+ * other bounded wait of the call uses the same limit.  A CTA whose wait runs
+ * out lets its loads and MMAs in flight finish, frees its tensor memory and
+ * sets status[stall_seq] = TS_ERR_TIMEOUT; CTAs with fewer tiles run to the
+ * end.  The outputs of that sequence are then unspecified; the other
+ * sequences' outputs are those of tree_attn_fwd (with a limit far above
+ * their run time), and the device stays usable.
+ * Returns TS_ERR_SHAPE for stall_seq outside [0, B) or stall_tile < 0,
+ * TS_ERR_UNSUPPORTED for wait_limit_us outside [100, 10^6], else as
+ * tree_attn_fwd.
+ */
+TS_API ts_status tree_attn_fwd_stall_test(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
+                                          int stall_seq, int stall_tile, uint32_t wait_limit_us,
+                                          ts_stream stream);
+
+/*
  * Bytes of device workspace tree_verify_greedy needs (a packed argmax key per
  * node and an arrival counter per sequence).  Host-only.
  */

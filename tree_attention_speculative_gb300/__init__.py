@@ -57,7 +57,7 @@ _LIB: Optional[ctypes.CDLL] = None
 EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_plan", "tree_attn_fwd",
            "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc",
            "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic", "tree_build_ancestry_forest",
-           "tree_verify_greedy_forest")
+           "tree_verify_greedy_forest", "tree_attn_fwd_stall_test")
 
 # TS_VERIFY_NOALLOC_SCRATCH_BYTES of treespec.h
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.tree_attn_plan.restype = i32
         L.tree_attn_fwd.argtypes = [ctypes.POINTER(AttnParams), vp, sz, vp]
         L.tree_attn_fwd.restype = i32
+        L.tree_attn_fwd_stall_test.argtypes = [ctypes.POINTER(AttnParams), vp, sz, i32, i32, ctypes.c_uint32, vp]
+        L.tree_attn_fwd_stall_test.restype = i32
         L.tree_verify_workspace_size.argtypes = [i32, i32, i32]
         L.tree_verify_workspace_size.restype = sz
         L.tree_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -176,6 +178,15 @@ def tree_attn_plan(params: AttnParams) -> dict:
 def tree_attn_fwd(params: AttnParams, workspace: torch.Tensor, stream=None) -> None:
     _check(lib().tree_attn_fwd(ctypes.byref(params), _p(workspace), workspace.numel() * workspace.element_size(),
                                _s(stream)), "tree_attn_fwd")
+
+
+def tree_attn_fwd_stall_test(params: AttnParams, workspace: torch.Tensor, stall_seq: int, stall_tile: int,
+                             wait_limit_us: int, stream=None) -> None:
+    """Testing only: tree_attn_fwd with sequence ``stall_seq``'s key stream
+    stopped before tile ``stall_tile``, so its bounded wait runs out."""
+    _check(lib().tree_attn_fwd_stall_test(ctypes.byref(params), _p(workspace),
+                                          workspace.numel() * workspace.element_size(), stall_seq, stall_tile,
+                                          wait_limit_us, _s(stream)), "tree_attn_fwd_stall_test")
 
 
 def tree_verify_workspace_size(B: int, N: int, V: int) -> int:

@@ -228,8 +228,12 @@ ts_status tree_attn_plan(const ts_attn_params* p, int32_t* chunk_tiles, int32_t*
   return TS_OK;
 }
 
-ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
-                        ts_stream stream) {
+}  // extern "C"
+
+namespace ts {
+namespace {
+ts_status attn_fwd_impl(const ts_attn_params* p, void* workspace, size_t workspace_bytes, ts_stream stream,
+                        int stall_seq, int stall_tile, unsigned long long wait_limit_ns) {
   ts_status st = check_attn(p);
   if (st != TS_OK) return st;
   const AttnPlan pl = plan_attn(p);
@@ -259,12 +263,32 @@ ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspa
   a.max_splits = pl.max_splits;
   a.tree_split = pl.tree_split;
   a.row_tiles = pl.row_tiles;
+  a.wait_limit_ns = wait_limit_ns;
+  a.stall_seq = stall_seq;
+  a.stall_tile = stall_tile;
   cudaStream_t s = (cudaStream_t)stream;
   if (prepare_device() != cudaSuccess) return TS_ERR_CUDA;
   if (launch_attn_tc(a, s) != cudaSuccess) return TS_ERR_CUDA;
   // with one split per unit the kernel writes `out` itself; otherwise merge the splits
   if (a.max_splits > 1 && launch_combine(a, s) != cudaSuccess) return TS_ERR_CUDA;
   return TS_OK;
+}
+}  // namespace
+}  // namespace ts
+
+extern "C" {
+
+ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
+                        ts_stream stream) {
+  return ts::attn_fwd_impl(p, workspace, workspace_bytes, stream, -1, 0, ATTN_WAIT_LIMIT_NS);
+}
+
+ts_status tree_attn_fwd_stall_test(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
+                                   int stall_seq, int stall_tile, uint32_t wait_limit_us, ts_stream stream) {
+  if (p && (stall_seq < 0 || stall_seq >= p->B || stall_tile < 0)) return TS_ERR_SHAPE;
+  if (wait_limit_us < 100 || wait_limit_us > 1000000) return TS_ERR_UNSUPPORTED;
+  return ts::attn_fwd_impl(p, workspace, workspace_bytes, stream, stall_seq, stall_tile,
+                           (unsigned long long)wait_limit_us * 1000ull);
 }
 
 size_t tree_verify_workspace_size(int B, int N, int V) {

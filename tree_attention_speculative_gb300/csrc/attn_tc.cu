@@ -42,8 +42,11 @@
 // does not wait for the PV that frees the buffer it needs next.
 // The tree block rides on the last prefix split of a unit or, when the host
 // plans it so, on a split of its own that runs beside the prefix splits.
-// Every mbarrier wait is bounded; a timeout sets a shared abort flag, every
-// role winds down, the CTA frees its TMEM and reports TS_ERR_TIMEOUT.
+// Every mbarrier wait is bounded; a timeout sets a shared abort flag and every
+// role winds down.  Before the CTA frees its TMEM and exits, an aborted CTA
+// drains what it still has in flight: the producers wait (bounded) for the
+// loads they issued to land, and each MMA issuer commits to a barrier of its
+// own and waits for its MMAs to finish.  It then reports TS_ERR_TIMEOUT.
 #include "fastexp.cuh"
 #include "internal.cuh"
 #include "sm100.cuh"
@@ -64,7 +67,6 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_O = 0;
 constexpr uint32_t TMEM_S0 = 128;
 constexpr int NSB = 3;  // S buffers in TMEM
-constexpr uint64_t WAIT_LIMIT_NS = 200000000ull;   // 200 ms: far above any legitimate wait
 // O is rescaled only when a row's max rises by more than 2^20 (log2 units).
 // Until then p = 2^(s - m_run) <= 2^20: bf16 P (range to 3e38) and the fp32 O
 // and l accumulators (relative precision independent of scale) stay exact up
@@ -97,6 +99,7 @@ struct __align__(1024) Smem {
   uint64_t p_full[NSB];
   uint64_t s_free[NSB];  // S buffer b no longer read: PV of its last tile completed
   uint64_t o_ready;
+  uint64_t drain[2];  // an aborted CTA's QK and PV issuers wait here for their MMAs
   uint32_t tmem_base;
   int abort_flag;
   int pv_done;  // PVs completed so far, published by the PV issuer (release/acquire)
@@ -109,13 +112,13 @@ struct TcArgs {
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > limit) {
       *abort_flag = 1;
       return false;
     }
@@ -123,7 +126,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 }
 
 // Bounded wait until the published PV count reaches `target`.
-__device__ __forceinline__ bool wait_count(const int* counter, int target, volatile int* abort_flag) {
+__device__ __forceinline__ bool wait_count(const int* counter, int target, volatile int* abort_flag, uint64_t limit) {
   const uint32_t addr = smem_u32(counter);
   auto load = [&]() {
     int v;
@@ -135,7 +138,7 @@ __device__ __forceinline__ bool wait_count(const int* counter, int target, volat
   while (true) {
     if (load() >= target) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > limit) {
       *abort_flag = 1;
       return false;
     }
@@ -166,6 +169,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const AttnArgs& a = args.a;
   volatile int* abort_flag = &sm.abort_flag;
+  const uint64_t limit = a.wait_limit_ns;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rt = blockIdx.x, split = blockIdx.y, unit = blockIdx.z;
@@ -210,6 +214,8 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       mbar_init(&sm.s_free[i], 1);
     }
     mbar_init(&sm.o_ready, 1);
+    mbar_init(&sm.drain[0], 1);
+    mbar_init(&sm.drain[1], 1);
     fence_barrier_init();
   }
   if (warp == PRODUCER_WARP) tmem_alloc(&sm.tmem_base, TMEM_COLS);
@@ -253,8 +259,9 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   // One warp streams the K tiles, another the V tiles: a single warp issues a
   // TMA request only every ~120 cycles, so one warp alone could not keep up
   // with 16 paged boxes per tile.  Each ring slot is refilled as soon as its
-  // own consumer (QK for K, PV for V) has released it.
-  auto kv_producer = [&](bool is_v) {
+  // own consumer (QK for K, PV for V) has released it.  Returns how many
+  // tiles it issued (all of them unless a wait gave up or a stall was asked for).
+  auto kv_producer = [&](bool is_v) -> int {
     const CUtensorMap* tm_pool = is_v ? &tm_vc : &tm_kc;
     const CUtensorMap* tm_node = is_v ? &tm_vt : &tm_kt;
     uint64_t* full = is_v ? sm.v_full : sm.k_full;
@@ -277,11 +284,14 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     };
     int grp_cur = load_group(0);
     int grp_nxt = (n_prefix > tpg) ? load_group(1) : 0;
-    for (int j = 0; j < n_tiles; ++j) {
+    const int stop = (!is_v && b == a.stall_seq) ? a.stall_tile : n_tiles;
+    int j = 0;
+    for (; j < n_tiles; ++j) {
       const int slot = j % C::NST;
       uint8_t* dst = is_v ? sm.v[slot] : sm.k[slot];
-      if (j >= C::NST && !__all_sync(0xffffffffu, wait_bar(&empty[slot], ((j / C::NST) - 1) & 1, abort_flag)))
+      if (j >= C::NST && !__all_sync(0xffffffffu, wait_bar(&empty[slot], ((j / C::NST) - 1) & 1, abort_flag, limit)))
         break;
+      if (j == stop) break;
       if (j < n_prefix) {
         if (j > 0 && j % tpg == 0) {
           grp_cur = grp_nxt;
@@ -306,7 +316,9 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       }
       __syncwarp();
     }
+    return j;
   };
+  int issued = 0;  // tiles this warp's producer issued (K or V), for the drain of an aborted CTA
 
   if (!has_work) {
     // nothing to do; fall through to the teardown
@@ -318,21 +330,21 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       for (int h = 0; h < C::HALVES; ++h)
         tma_load_4d(sm.q + h * (ROW_TILE * 128), &tm_q, &sm.q_full, 64 * h, g * a.G, rt * nodes_per_tile, b);
     }
-    kv_producer(false);
+    issued = kv_producer(false);
   } else if (warp == V_PRODUCER_WARP) {
-    kv_producer(true);
+    issued = kv_producer(true);
   } else if (warp == QK_WARP) {
     // ------------------------------------------------------------ QK issuer
     if (lane == 0) {
       constexpr uint32_t ID_QK = idesc_bf16_f32(128, KV_TILE, 0, 0);
       const uint32_t q_addr = smem_u32(sm.q);
-      bool ok = wait_bar(&sm.q_full, 0, abort_flag);
+      bool ok = wait_bar(&sm.q_full, 0, abort_flag, limit);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int slot = j % C::NST;
         // K(j) has landed; S buffer j%3 is free once PV(j-3) has completed
         // (a per-buffer barrier: it can never run two completions ahead)
-        ok = wait_bar(&sm.k_full[slot], (j / C::NST) & 1, abort_flag) &&
-             (j < NSB || wait_bar(&sm.s_free[j % NSB], ((j / NSB) - 1) & 1, abort_flag));
+        ok = wait_bar(&sm.k_full[slot], (j / C::NST) & 1, abort_flag, limit) &&
+             (j < NSB || wait_bar(&sm.s_free[j % NSB], ((j / NSB) - 1) & 1, abort_flag, limit));
         if (!ok) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm.k[slot]);
@@ -359,8 +371,8 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       constexpr uint32_t ID_PV = idesc_bf16_f32(128, D, 0, 1);
       for (int j = 0; j < n_tiles; ++j) {
         const int slot = j % C::NST;
-        if (!wait_bar(&sm.p_full[j % NSB], (j / NSB) & 1, abort_flag)) break;
-        if (!wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag)) break;
+        if (!wait_bar(&sm.p_full[j % NSB], (j / NSB) & 1, abort_flag, limit)) break;
+        if (!wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag, limit)) break;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sm.v[slot]);
         const uint32_t p_tmem = tmem + TMEM_S0 + (j % NSB) * 128;
@@ -376,7 +388,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         mma_commit(&sm.v_empty[slot]);  // V(j) no longer read
         // wait for PV(j) here (every phase in order) and publish the count, so
         // the softmax looks at O only when it has to rescale it
-        if (!wait_bar(&sm.o_ready, j & 1, abort_flag)) break;
+        if (!wait_bar(&sm.o_ready, j & 1, abort_flag, limit)) break;
         tc_fence_after();
         asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.pv_done)), "r"(j + 1) : "memory");
       }
@@ -401,7 +413,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     float m_run = NEG_INF, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      if (!__all_sync(0xffffffffu, wait_bar(&sm.s_full[j % NSB], (j / NSB) & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, wait_bar(&sm.s_full[j % NSB], (j / NSB) & 1, abort_flag, limit))) {
         ok = false;
         break;
       }
@@ -494,7 +506,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         // rows >= valid of this V tile hold whatever the pool had past the
         // prefix (or stale data): zero them so 0 * V can never be NaN
         const int slot = j % C::NST;
-        if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag, limit))) {
           ok = false;
           break;
         }
@@ -511,7 +523,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         // O must hold PV(0..j-1) complete before it is rescaled.  TMEM loads
         // and stores are warp-collective: the whole warp rescales its rows
         // together, with factor 1 for rows whose max did not move enough.
-        if (!__all_sync(0xffffffffu, wait_count(&sm.pv_done, j, abort_flag))) {
+        if (!__all_sync(0xffffffffu, wait_count(&sm.pv_done, j, abort_flag, limit))) {
           ok = false;
           break;
         }
@@ -547,7 +559,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     // k ^ (r % 8): the 128-byte swizzle, and conflict-free for these writes),
     // then one thread stores the boxes.  The K ring is idle by now: every QK
     // has completed before the last PV could start.
-    const bool epi = ok && __all_sync(0xffffffffu, wait_count(&sm.pv_done, n_tiles, abort_flag));
+    const bool epi = ok && __all_sync(0xffffffffu, wait_count(&sm.pv_done, n_tiles, abort_flag, limit));
     uint8_t* stage = &sm.k[0][0];
     float lse2 = 0.f;
     if (epi) {
@@ -605,6 +617,23 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
 
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // A wait gave up.  Nothing may still write this CTA's shared memory or
+    // TMEM once it exits: wait (bounded, regardless of the flag) for the last
+    // loads each producer issued (only the newest NST tiles of a ring can be
+    // outstanding) and for every MMA each issuer started.
+    if ((warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && lane == 0) {
+      uint64_t* full = warp == PRODUCER_WARP ? sm.k_full : sm.v_full;
+      if (warp == PRODUCER_WARP && has_work) mbar_wait(&sm.q_full, 0, limit);
+      for (int j = max(0, issued - C::NST); j < issued; ++j) mbar_wait(&full[j % C::NST], (j / C::NST) & 1, limit);
+    } else if ((warp == QK_WARP || warp == PV_WARP) && lane == 0) {
+      uint64_t* d = &sm.drain[warp - QK_WARP];
+      mma_commit(d);
+      mbar_wait(d, 0, limit);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   pdl_trigger();
   if (sm.abort_flag && threadIdx.x == 0 && a.status) a.status[b] = TS_ERR_TIMEOUT;
   if (warp == PRODUCER_WARP) {

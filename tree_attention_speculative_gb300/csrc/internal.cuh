@@ -94,7 +94,14 @@ struct AttnArgs {
   int max_splits;    // splits of the longest sequence, the tree's own split included
   int tree_split;    // 1: the tree block is a split of its own
   int row_tiles;     // ceil(N*G / ROW_TILE)
+  // Every bounded wait of the attention kernel gives up after wait_limit_ns.
+  // Testing the failure path: with stall_seq >= 0, every CTA of that sequence
+  // stops its K stream before tile stall_tile (its loads are never issued),
+  // so the wait for that tile runs out with nothing in flight.
+  unsigned long long wait_limit_ns;
+  int stall_seq, stall_tile;
 };
+constexpr unsigned long long ATTN_WAIT_LIMIT_NS = 200000000ull;  // 200 ms: far above any legitimate wait
 
 struct AttnPlan {
   int chunk_tiles;
