@@ -1,24 +1,31 @@
 """Benchmark of one tree-attention speculative verification step on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload c2]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload c4]
+                    [--sub c3,c5,c2,c1]
 
 A step is one pass of the whole hot path over one batch of synthetic input:
 tree_build_ancestry -> tree_attn_fwd -> tree_verify_greedy.  The metric is tree
 tokens verified per second (B * N / step time).  Prints ONE JSON line.
 
+The headline workload is c4, the 70B-shaped layer (batch 64, 64-node trees,
+8192-token paged prefixes, vocab 128256), the largest configuration; the
+line also carries sub-records for c3 (batched serving), c5 (131072-token
+prefixes), c2 and c1, each with its step time, per-call times and rooflines.
+
 Timing (impl=ours): the K timed steps are captured into CUDA graphs (chunks of
 S steps) and replayed back to back; the whole timed region is bracketed by a
 barrier and a synchronize, with CUDA events on the launching stream around it.
 The library's kernels use programmatic dependent launch, so a graph with event
-nodes between the kernels would serialise them; the per-kernel durations are
+nodes between the kernels would serialise them; the per-call durations are
 therefore taken in a second region right after, from a graph of the same
-steps with a timing event node around every library call.  Steps rotate over
-several independent input sets whose union is larger than the 129 MB L2, so
-every step reads its inputs from HBM.  ``e2e``
-repeats the step through the same public calls from pinned host buffers, with
-the host->device copies of all inputs and the device->host read of the
-accepted path inside the timed region.  ``cpu_baseline`` (and impl=reference)
-time the CPU oracle on a bounded sample of the same workload.
+steps with a timing event node around every library call.  Where one input
+set is smaller than twice the 129 MB L2, steps rotate over several
+independent sets whose union is larger, so every step reads its inputs from
+HBM.  ``e2e`` repeats the headline step through the same public calls from
+pinned host buffers, with the host->device copies of all inputs and the
+device->host read of the accepted path inside the timed region.
+``cpu_baseline`` (and impl=reference) time the CPU oracle on bounded samples
+of the same workloads.
 
 Under torchrun (--gpus N > 1) every rank runs an independent replica of the
 workload on its own GPU (the path has no exchange step); rank 0 prints the
@@ -211,35 +218,26 @@ def barrier(world: int):
 
 # ----------------------------------------------------------------------------- oracle timing
 
-def oracle_sample_step(case):
-    """One bounded oracle step: ancestry of every tree, attention of ONE
-    (sequence, kv-head) unit, argmax of a few logit rows and one acceptance
-    walk.  Returns (full-step seconds extrapolated by unit and row counts,
-    seconds actually spent, description of the sample)."""
+def oracle_part(case, seqs, units):
+    """Run the oracle on part of one step and return the seconds it took:
+    ancestry of the trees of ``seqs``, attention of the (sequence, kv-head)
+    ``units``, and (with logits) the argmax of every row of ``seqs`` plus
+    their acceptance walks."""
     import oracle
-    units_total = case.B * case.Hkv
-    rows_total = case.B * case.N
-    t0 = time.perf_counter()
+    import workloads as W
+    seqs = list(seqs)
     forest = bool((case.parent[:, 1:] < 0).any())
-    (oracle.forest.build_ancestry_forest if forest else oracle.tree.build_ancestry)(case.parent, case.prefix_len)
-    t1 = time.perf_counter()
-    oracle.attention.tree_attention_case(case, units=[(0, 0)])
-    t2 = time.perf_counter()
-    t_ver = 0.0
-    vrows = 0
+    t0 = time.perf_counter()
+    (oracle.forest.build_ancestry_forest if forest else oracle.tree.build_ancestry)(case.parent[seqs],
+                                                                                   case.prefix_len[seqs])
+    if units:
+        oracle.attention.tree_attention_case(case, units=list(units))
     if case.vocab:
-        vrows = min(rows_total, 8)
-        lg = case.logits.reshape(rows_total, case.vocab)[:vrows]
-        oracle.verify.greedy_argmax(lg)
-        am = oracle.verify.greedy_argmax(case.logits[0])
-        (oracle.forest.accept_walk_forest if forest else oracle.verify.accept_walk)(case.parent[0], case.draft[0], am,
-                                                                                    case.N)
-        t_ver = time.perf_counter() - t2
-    full = (t1 - t0) + (t2 - t1) * units_total + (t_ver * rows_total / max(vrows, 1) if vrows else 0.0)
-    desc = (f"ancestry of all {case.B} trees; attention of 1 of {units_total} (sequence, kv-head) units x "
-            f"{units_total}; argmax of {vrows} of {rows_total} logit rows (+ one acceptance walk) x "
-            f"{rows_total // max(vrows, 1)}")
-    return full, (t2 - t0) + t_ver, desc
+        am = oracle.verify.greedy_argmax(case.logits[seqs])
+        walk = oracle.forest.accept_walk_forest if forest else oracle.verify.accept_walk
+        for i, b in enumerate(seqs):
+            walk(case.parent[b], case.draft[b], am[i], W.LEVELS.get(case.name, case.N - 1))
+    return time.perf_counter() - t0
 
 
 def blas_threads():
@@ -253,49 +251,79 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def time_oracle(case, budget_s: float, steps: int = 0):
-    """Repeat the bounded oracle step for about ``budget_s`` seconds (or exactly
-    ``steps`` times); tokens/s = B*N / extrapolated full-step time."""
-    est = []
-    spent = 0.0
-    desc = ""
-    n = 0
-    while (steps and n < steps) or (not steps and (spent < budget_s or n < 1)):
-        full, wall, desc = oracle_sample_step(case)
-        est.append(full)
-        spent += wall
-        n += 1
-    t = float(np.median(est))
-    return case.B * case.N / t, t, desc, n
+def _one_thread():
+    try:
+        from threadpoolctl import threadpool_limits
+        return threadpool_limits(1)
+    except Exception:   # pragma: no cover
+        import contextlib
+        return contextlib.nullcontext()
+
+
+def oracle_throughput(case, budget_s: float, mode: str):
+    """Tree tokens verified per second by the CPU oracle on ``case``.
+
+    mode "full": the whole step (every tree, every unit, every row), repeated
+    until ``budget_s`` is spent.  mode "sequences": whole sequences, one after
+    another from sequence 0, until ``budget_s`` is spent; nothing is
+    extrapolated (tokens = the sequences' nodes).  mode "units": ancestry and
+    verification of the whole batch plus attention of seeded (sequence,
+    kv-head) units until ``budget_s`` is spent, the attention time scaled by
+    the unit count (stated in the sample).  Returns (tokens/s, description)."""
+    B, N, Hkv = case.B, case.N, case.Hkv
+    allu = [(b, g) for b in range(B) for g in range(Hkv)]
+    if mode == "full":
+        ts = []
+        while not ts or sum(ts) < budget_s:
+            ts.append(oracle_part(case, range(B), allu))
+        t = float(np.median(ts))
+        return B * N / t, f"the whole step (all {B} trees, {B * Hkv} units, {B * N} rows), median of {len(ts)}"
+    if mode == "sequences":
+        spent, seqs = 0.0, 0
+        while seqs < B and (seqs == 0 or spent < budget_s):
+            spent += oracle_part(case, [seqs], [(seqs, g) for g in range(Hkv)])
+            seqs += 1
+        return seqs * N / spent, (f"sequences 0..{seqs - 1} of {B}, each whole (ancestry, attention of all "
+                                  f"{Hkv} kv heads, argmax of its {N} rows, walk); {spent:.1f} s, no extrapolation")
+    # units
+    t_rest = oracle_part(case, range(B), [])
+    g = np.random.default_rng(12345)
+    order = [allu[i] for i in g.permutation(len(allu))]
+    spent, k = 0.0, 0
+    while k < len(order) and (k == 0 or spent < budget_s):
+        spent += oracle_part(case, [order[k][0]], [order[k]])
+        k += 1
+    # each unit's call also re-ran its sequence's ancestry/argmax/walk: remove that share
+    t_unit = max(spent / k - t_rest / B, 1e-9)
+    t = t_rest + t_unit * len(allu)
+    return B * N / t, (f"ancestry, argmax and walks of all {B} sequences ({t_rest:.2f} s) + attention of {k} "
+                       f"seeded of {len(allu)} (sequence, kv-head) units ({t_unit:.2f} s each, net of their "
+                       f"sequence's verify), extrapolated x{len(allu)}")
+
+
+CPU_MODES = {"c1": "full", "c2": "full", "c3": "full", "c4": "sequences", "c5": "units"}
 
 
 # ----------------------------------------------------------------------------- GPU bench
 
-def run_ours(args, world, rank, local):
+def measure_gpu(name, args, dev, world, K, overrides, with_e2e=False, sampler=None, warmup=5):
+    """Time K steps of workload ``name`` (graph-captured, barrier + synchronize
+    on both sides, CUDA events, max over ranks) and each library call's share;
+    optionally the e2e step from pinned host buffers.  Returns a record."""
     import torch
     import workloads as W
-    from tree_attention_speculative_gb300 import _build
-    _build.build()
-    from tree_attention_speculative_gb300.step import TreeVerifyStep
+    from tree_attention_speculative_gb300.step import PackedInputs, TreeVerifyStep
     from tests.gpu_util import to_dev
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    base = W.make(args.workload, **workload_overrides(args))
+    base = W.make(name, **overrides)
     set_bytes = sum(x.nbytes for x in (base.q, base.k_cache, base.v_cache, base.k_tree, base.v_tree)) + \
         (base.logits.nbytes if base.logits is not None else 0)
     nsets = max(1, min(16, math.ceil(2 * L2_BYTES / set_bytes))) if set_bytes < 2 * L2_BYTES else 1
-    cases = [base] + [W.make(args.workload, seed=20270000 + 97 * k, **workload_overrides(args))
-                      for k in range(1, nsets)]
+    cases = [base] + [W.make(name, seed=20270000 + 97 * k, **overrides) for k in range(1, nsets)]
     dsets = [to_dev(c, dev) for c in cases]
-    # one set of output buffers per input set (prefix lengths, hence the split plan, may differ)
-    steps = [TreeVerifyStep(c.B, c.N, c.Hq, c.Hkv, c.D, c.prefix_len, vocab=c.vocab, max_depth=c.N - 1,
-                            device=dev, forest=bool(args.forest)) for c in cases]
-    step = steps[0]
+    forest = bool(overrides.get("forest_roots"))
+    steps = [TreeVerifyStep(c.B, c.N, c.Hq, c.Hkv, c.D, c.prefix_len, vocab=c.vocab,
+                            max_depth=W.LEVELS.get(name, c.N - 1), device=dev, forest=forest) for c in cases]
 
     def enqueue(k, evs=None):
         enqueue_on(dsets[k % nsets], steps[k % nsets], evs)
@@ -311,49 +339,32 @@ def run_ours(args, world, rank, local):
             st.verify(t["draft"], t["logits"], t["parent"])
         if evs: evs[3].record()
 
-    # allocate workspaces eagerly, then warm up
-    for k in range(nsets):
+    for k in range(nsets):    # allocate workspaces eagerly
         enqueue(k)
     torch.cuda.synchronize()
-    for k in range(args.warmup):
+    for k in range(warmup):
         enqueue(k)
     torch.cuda.synchronize()
 
-    K = args.steps
     S = min(K, max(nsets, 8 * nsets))
     S = S - S % nsets if S >= nsets else S
     stream = torch.cuda.Stream(device=dev)
 
-    def capture(nsteps):
+    def capture(nsteps, timed_calls):
         g = torch.cuda.CUDAGraph()
         evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(nsteps)]
         with torch.cuda.graph(g, stream=stream):
             for k in range(nsteps):
-                enqueue(k, evs[k])
+                enqueue(k, evs[k] if timed_calls else None)
         return g, evs
 
-    def capture_plain(nsteps):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(nsteps):
-                enqueue(k)
-        return g
-
     full, last = divmod(K, S)
-    g_main = capture_plain(S) if full else None
-    g_rem = capture_plain(last) if last else None
-    # one untimed replay of each graph uploads it
-    if g_main: g_main.replay()
+    g_main = capture(S, False)[0] if full else None
+    g_rem = capture(last, False)[0] if last else None
+    if g_main: g_main.replay()    # one untimed replay of each graph uploads it
     if g_rem: g_rem.replay()
     torch.cuda.synchronize()
 
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        gpu_id = str(local)
-    sampler = ClockSampler(gpu_id)
-    sampler.start()
-    time.sleep(0.3)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -369,15 +380,11 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     w1 = time.time()
     barrier(world)
-    time.sleep(0.2)
-    sampler.stop()
-    ms_total = e0.elapsed_time(e1)
-    ms_total = max_over_ranks(ms_total, world, dev)
-    ms_step = ms_total / K
+    ms_step = max_over_ranks(e0.elapsed_time(e1), world, dev) / K
 
-    # per-kernel durations: the same steps with an event node around every call
+    # per-call durations: the same steps again, with an event node around every call
     S_ev = min(K, S)
-    g_ev, evs = capture(S_ev)
+    g_ev, evs = capture(S_ev, True)
     g_ev.replay()
     torch.cuda.synchronize()
     g_ev.replay()
@@ -389,142 +396,224 @@ def run_ours(args, world, rank, local):
         if base.vocab:
             per["tree_verify_greedy"].append(e[2].elapsed_time(e[3]))
     kern_ms = {k: float(np.mean(v)) for k, v in per.items() if v}
-
-    # kernels per step: ancestry, attention, combine when the prefix is split, verify
     ws_attn = steps[0].ws_attn.numel() if steps[0].ws_attn is not None else 0
     kernels_per_step = 2 + (1 if ws_attn > 256 else 0) + (1 if base.vocab else 0)
-    # the timed steps must have run clean
     for st in steps:
-        assert (st.status.cpu().numpy() == 0).all(), "timed step reported an error status"
+        assert (st.status.cpu().numpy() == 0).all(), f"{name}: a timed step reported an error status"
+    del g_main, g_rem, g_ev
 
-    # ---------------- e2e through the public calls, from pinned host buffers
-    # Each input set is packed into one pinned host buffer (PackedInputs), so a
-    # step's whole upload is one copy.  Uploads run on a copy stream: step k+1's
-    # upload overlaps step k's kernels, and an upload into a set waits until
-    # the kernels that last read that set are done.  Every step's upload and
-    # its result read-back are inside the timed region.
-    import torch as _t
-    from tree_attention_speculative_gb300.step import PackedInputs
+    rec = {"name": name, "case": base, "K": K, "ms_step": ms_step, "kern_ms": kern_ms, "w0": w0, "w1": w1,
+           "S": S, "S_ev": S_ev, "nsets": nsets, "set_bytes": set_bytes, "kernels_per_step": kernels_per_step}
 
-    def host_arrays(c):
-        h = {}
-        for name, arr in (("parent", c.parent), ("prefix_len", c.prefix_len), ("block_table", c.block_table)):
-            h[name] = _t.from_numpy(np.ascontiguousarray(arr, np.int32))
-        for name in ("q", "k_cache", "v_cache", "k_tree", "v_tree"):
-            h[name] = _t.from_numpy(np.ascontiguousarray(getattr(c, name)).view(np.int16)).view(_t.bfloat16)
-        if c.vocab:
-            h["draft"] = _t.from_numpy(np.ascontiguousarray(c.draft, np.int32))
-            h["logits"] = _t.from_numpy(np.ascontiguousarray(c.logits, np.float32))
-        return h
+    if with_e2e:
+        # e2e through the public calls.  Each input set is packed into one
+        # pinned host buffer (PackedInputs), so a step's whole upload is one
+        # copy; uploads run on a copy stream, step k+1's overlapping step k's
+        # kernels, and an upload into a set waits until the kernels that last
+        # read it are done.  Every step's upload and its result read-back are
+        # inside the timed region.
+        def host_arrays(c):
+            h = {}
+            for nm, arr in (("parent", c.parent), ("prefix_len", c.prefix_len), ("block_table", c.block_table)):
+                h[nm] = torch.from_numpy(np.ascontiguousarray(arr, np.int32))
+            for nm in ("q", "k_cache", "v_cache", "k_tree", "v_tree"):
+                h[nm] = torch.from_numpy(np.ascontiguousarray(getattr(c, nm)).view(np.int16)).view(torch.bfloat16)
+            if c.vocab:
+                h["draft"] = torch.from_numpy(np.ascontiguousarray(c.draft, np.int32))
+                h["logits"] = torch.from_numpy(np.ascontiguousarray(c.logits, np.float32))
+            return h
 
-    packs = [PackedInputs(host_arrays(c), dev) for c in cases]
-    pviews = [{name: p.device(name) for name in p.layout} for p in packs]
-    outs = {"accepted": _t.empty((base.B, base.N), dtype=_t.int32).pin_memory(),
-            "accept_len": _t.empty(base.B, dtype=_t.int32).pin_memory(),
-            "bonus": _t.empty(base.B, dtype=_t.int32).pin_memory(),
-            "status": _t.empty(base.B, dtype=_t.int32).pin_memory()}
-    h2d = packs[0].nbytes
-    d2h = sum(v.numel() * v.element_size() for v in outs.values())
-    K_e2e = min(K, max(3 * nsets, int(2.0e-3 * K) + 3 * nsets)) if K > 200 else K
-    copy_stream = _t.cuda.Stream(device=dev)
-    copied = [_t.cuda.Event() for _ in range(nsets)]
-    consumed = [_t.cuda.Event() for _ in range(nsets)]
+        packs = [PackedInputs(host_arrays(c), dev) for c in cases]
+        pviews = [{nm: pk.device(nm) for nm in pk.layout} for pk in packs]
+        outs = {"accepted": torch.empty((base.B, W.LEVELS.get(name, base.N - 1) + 1), dtype=torch.int32).pin_memory(),
+                "accept_len": torch.empty(base.B, dtype=torch.int32).pin_memory(),
+                "bonus": torch.empty(base.B, dtype=torch.int32).pin_memory(),
+                "status": torch.empty(base.B, dtype=torch.int32).pin_memory()}
+        h2d = packs[0].nbytes
+        d2h = sum(v.numel() * v.element_size() for v in outs.values())
+        K_e2e = min(K, max(3 * nsets, int(2.0e-3 * K) + 3 * nsets)) if K > 200 else K
+        copy_stream = torch.cuda.Stream(device=dev)
+        copied = [torch.cuda.Event() for _ in range(nsets)]
+        consumed = [torch.cuda.Event() for _ in range(nsets)]
 
-    def e2e_step(k):
-        i = k % nsets
-        main = _t.cuda.current_stream(dev)
-        copy_stream.wait_event(consumed[i])
-        packs[i].upload(copy_stream)
-        copied[i].record(copy_stream)
-        main.wait_event(copied[i])
-        enqueue_on(pviews[i], steps[i])
-        consumed[i].record(main)
-        st = steps[i]
-        if base.vocab:
-            outs["accepted"].copy_(st.accepted, non_blocking=True)
-            outs["accept_len"].copy_(st.accept_len, non_blocking=True)
-            outs["bonus"].copy_(st.bonus, non_blocking=True)
-        outs["status"].copy_(st.status, non_blocking=True)
+        def e2e_step(k):
+            i = k % nsets
+            main = torch.cuda.current_stream(dev)
+            copy_stream.wait_event(consumed[i])
+            packs[i].upload(copy_stream)
+            copied[i].record(copy_stream)
+            main.wait_event(copied[i])
+            enqueue_on(pviews[i], steps[i])
+            consumed[i].record(main)
+            st = steps[i]
+            if base.vocab:
+                outs["accepted"].copy_(st.accepted, non_blocking=True)
+                outs["accept_len"].copy_(st.accept_len, non_blocking=True)
+                outs["bonus"].copy_(st.bonus, non_blocking=True)
+            outs["status"].copy_(st.status, non_blocking=True)
 
-    for k in range(min(3, K_e2e)):
-        e2e_step(k)
+        for k in range(min(3, K_e2e)):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        x0 = torch.cuda.Event(enable_timing=True)
+        x1 = torch.cuda.Event(enable_timing=True)
+        x0.record()
+        copy_stream.wait_stream(torch.cuda.current_stream(dev))
+        for k in range(K_e2e):
+            e2e_step(k)
+        torch.cuda.current_stream(dev).wait_stream(copy_stream)
+        x1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_e2e = max_over_ranks(x0.elapsed_time(x1), world, dev) / K_e2e
+        rec["e2e"] = {"value": world * base.B * base.N / (ms_e2e * 1e-3), "unit": "tree tokens/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K_e2e, "ms_per_step": ms_e2e,
+                      "staging": "each step's inputs in one pinned buffer, uploaded by one copy on a copy stream "
+                                 "that overlaps the previous step's kernels; results read back every step"}
+        del packs, pviews
+    del dsets, steps, cases
     torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    x0 = torch.cuda.Event(enable_timing=True)
-    x1 = torch.cuda.Event(enable_timing=True)
-    x0.record()
-    copy_stream.wait_stream(_t.cuda.current_stream(dev))
-    for k in range(K_e2e):
-        e2e_step(k)
-    _t.cuda.current_stream(dev).wait_stream(copy_stream)
-    x1.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    ms_e2e = max_over_ranks(x0.elapsed_time(x1), world, dev) / K_e2e
+    torch.cuda.empty_cache()
+    return rec
 
-    tokens = base.B * base.N
-    value = world * tokens / (ms_step * 1e-3)
-    e2e_value = world * tokens / (ms_e2e * 1e-3)
 
-    alg = algorithmic(base)
-    pk = peaks()
-    dom = max(kern_ms, key=kern_ms.get)
+def roofline_of(rec, pk, world=1):
+    """Per-call throughput against the measured peaks; the attention call gets
+    both its tensor and its HBM fraction.  Tensor fractions use the burst
+    bf16 peak: these calls run at the full SM clock, and the sustained figure
+    was taken under the power cap at a lower clock."""
+    alg = algorithmic(rec["case"])
+    kern = {}
+    for k, ms in rec["kern_ms"].items():
+        kb = alg[k]
+        gbs = kb["bytes"] / (ms * 1e-3) / 1e9
+        kern[k] = {"ms": ms, "share": ms / sum(rec["kern_ms"].values()), "GB/s": gbs, "hbm_frac": gbs / pk["hbm_gbs"]}
+        if kb["flops"]:
+            tf = kb["flops"] / (ms * 1e-3) / 1e12
+            kern[k]["TFLOP/s"] = tf
+            kern[k]["tensor_frac"] = tf / pk["bf16_tflops"]
+    dom = max(rec["kern_ms"], key=rec["kern_ms"].get)
     a = alg[dom]
-    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    t_dom = kern_ms[dom] * 1e-3
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     if a["flops"] and a["flops"] / max(a["bytes"], 1) > ridge:
-        roof = {"bound": "tensor", "achieved": a["flops"] / t_dom / 1e12, "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": kern[dom]["TFLOP/s"], "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": kern[dom]["tensor_frac"], "hbm_achieved_GBs": kern[dom]["GB/s"],
+                "hbm_frac": kern[dom]["hbm_frac"]}
     else:
-        roof = {"bound": "hbm", "achieved": a["bytes"] / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic(dom, args.workload)
+        roof = {"bound": "hbm", "achieved": kern[dom]["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": kern[dom]["hbm_frac"]}
+        if "TFLOP/s" in kern[dom]:
+            roof["tensor_achieved_TFs"] = kern[dom]["TFLOP/s"]
+            roof["tensor_frac"] = kern[dom]["tensor_frac"]
+    roof["traffic"] = recorded_traffic(dom, rec["name"])
     roof["kernel"] = dom
     roof["algorithmic_bytes"] = a["bytes"]
     roof["algorithmic_flops"] = a["flops"]
-    roof["peak_source"] = f"{pk['source']} ({'burst' if roof['unit'] == 'GB/s' else 'sustained'})"
+    roof["peak_source"] = f"{pk['source']} ({'hbm copy' if roof['unit'] == 'GB/s' else 'bf16 burst'})"
+    return roof, kern
 
-    kernels = {}
-    for k, ms in kern_ms.items():
-        kb = alg[k]
-        kernels[k] = {"ms": ms, "share": ms / sum(kern_ms.values()), "GB/s": kb["bytes"] / (ms * 1e-3) / 1e9,
-                      "hbm_frac": kb["bytes"] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
-        if kb["flops"]:
-            kernels[k]["TFLOP/s"] = kb["flops"] / (ms * 1e-3) / 1e12
 
+def workload_record(rec, pk, world, cpu=None):
+    """The sub-record of one workload inside the bench line."""
+    c = rec["case"]
+    roof, kern = roofline_of(rec, pk, world)
+    out = {"workload": f"{rec['name']}: " + WORKLOAD_DESC[rec["name"]],
+           "value": world * c.B * c.N / (rec["ms_step"] * 1e-3), "unit": "tree tokens/s",
+           "ms_per_step": rec["ms_step"], "steps": rec["K"], "roofline": roof, "kernels": kern,
+           "l2": l2_note(rec)}
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    return out
+
+
+def l2_note(rec):
+    tot = rec["nsets"] * rec["set_bytes"]
+    if tot > L2_BYTES:
+        return (f"{rec['nsets']} rotating input set(s) of {rec['set_bytes'] / 2**20:.1f} MiB "
+                f"({tot / 2**20:.0f} MiB > 129 MiB L2)")
+    return f"{rec['nsets']} input sets of {rec['set_bytes'] / 2**20:.2f} MiB: L2-resident (launch-bound case)"
+
+
+def cpu_record(case, budget_s, mode, one_thread_budget=None):
+    v, desc = oracle_throughput(case, budget_s, mode)
+    out = {"value": v, "unit": "tree tokens/s", "cores": blas_threads(), "kind": "oracle",
+           "sample": f"{desc}; numpy fp64 oracle, BLAS threads as reported"}
+    if one_thread_budget is not None:
+        with _one_thread():
+            v1, d1 = oracle_throughput(case, one_thread_budget, mode)
+        out["one_thread"] = {"value": v1, "cores": 1, "sample": d1}
+    return out
+
+
+SUB_STEPS = {"c1": 2000, "c2": 2000, "c3": 1000, "c4": 200, "c5": 100}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from tree_attention_speculative_gb300 import _build
+    _build.build()
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pk = peaks()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+
+    head = measure_gpu(args.workload, args, dev, world, args.steps, workload_overrides(args), with_e2e=True,
+                       warmup=args.warmup)
+    time.sleep(0.2)
+    subs = {}
+    for name in args.sub:
+        if name == args.workload:
+            continue
+        subs[name] = measure_gpu(name, args, dev, world, max(args.steps, SUB_STEPS[name]), {}, warmup=args.warmup)
+    sampler.stop()
+
+    base = head["case"]
+    roof, kern = roofline_of(head, pk, world)
     cpu = None
+    sub_cpu = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, t, desc, n = time_oracle(base, budget_s=args.cpu_budget)
-        cpu = {"value": v, "unit": "tree tokens/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{desc}; median of {n} repeats; numpy fp64 oracle, BLAS threads as reported"}
-
-    clocks = sampler.summary(w0, w1)
+        cpu = cpu_record(base, args.cpu_budget, CPU_MODES[args.workload],
+                         one_thread_budget=args.cpu_budget / 4)
+        for name, rec in subs.items():
+            mode = CPU_MODES[name]
+            sub_cpu[name] = cpu_record(rec["case"], 2.0 if mode == "full" else 4.0, mode,
+                                       one_thread_budget=(0.5 if mode == "full" else None))
     line = {
         "metric": "tree-verify step: tree tokens verified/s",
-        "value": value, "unit": "tree tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "value": world * base.B * base.N / (head["ms_step"] * 1e-3), "unit": "tree tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: " + WORKLOAD_DESC[args.workload] +
                                (f"; each tree replaced by a forest of {args.forest} trees" if args.forest else ""),
-                   "batch": base.B,
-                   "tree_nodes": base.N, "q_heads": base.Hq, "kv_heads": base.Hkv, "head_dim": base.D,
-                   "prefix": [int(x) for x in np.unique(base.prefix_len)][:4], "kv_block": base.bs,
-                   "vocab": base.vocab, "parallelism": f"replicas x{world}",
-                   "l2": f"{nsets} rotating input sets of {set_bytes / 2**20:.1f} MiB "
-                         f"({nsets * set_bytes / 2**20:.0f} MiB > 129 MiB L2)",
-                   "timing": f"CUDA graphs of {S} steps replayed back to back, CUDA events around the K steps; "
-                             f"per-kernel times from {S_ev} more steps with an event node around each call"},
+                   "batch": base.B, "tree_nodes": base.N, "q_heads": base.Hq, "kv_heads": base.Hkv,
+                   "head_dim": base.D, "prefix": [int(x) for x in np.unique(base.prefix_len)][:4],
+                   "kv_block": base.bs, "vocab": base.vocab, "parallelism": f"replicas x{world}",
+                   "l2": l2_note(head),
+                   "timing": f"CUDA graphs of {head['S']} steps replayed back to back, CUDA events around the K "
+                             f"steps; per-call times from {head['S_ev']} more steps with an event node around "
+                             f"each call"},
         "roofline": roof,
-        "kernels": kernels,
-        "e2e": {"value": e2e_value, "unit": "tree tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": K_e2e, "ms_per_step": ms_e2e,
-                "staging": "each step's inputs in one pinned buffer, uploaded by one copy on a copy stream "
-                           "that overlaps the previous step's kernels; results read back every step"},
-        "gpu_launches": K * kernels_per_step,
-        "clocks": clocks,
+        "kernels": kern,
+        "e2e": head["e2e"],
+        "gpu_launches": args.steps * head["kernels_per_step"],
+        "clocks": sampler.summary(head["w0"], head["w1"]),
         "cpu_baseline": cpu,
+        "workloads": {name: workload_record(rec, pk, world, sub_cpu.get(name)) for name, rec in subs.items()},
     }
+    for name, rec in subs.items():
+        line["workloads"][name]["clocks"] = sampler.summary(rec["w0"], rec["w1"])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -837,24 +926,49 @@ def run_dynamic(args, world, rank, local):
 
 
 def run_reference(args, world, rank):
-    """The oracle as the reference arm: rank 0 alone, on the host cores."""
+    """The oracle as the reference arm: rank 0 alone, on the host cores.  Each
+    step is one real, bounded piece of the workload, timed as run (no
+    extrapolation): one whole sequence (its ancestry, attention over every kv
+    head, argmax of its rows and its walk), or on c5, where a sequence takes
+    minutes, one (sequence, kv-head) unit plus that sequence's verification,
+    credited as N / Hkv tokens."""
     if rank != 0:
         return
     import workloads as W
     case = W.make(args.workload, **workload_overrides(args))
-    for _ in range(max(0, min(args.warmup, 1))):
-        oracle_sample_step(case)
+    B, N, Hkv = case.B, case.N, case.Hkv
+    per_unit = args.workload == "c5"
+
+    def step(k):
+        if per_unit:
+            b, g = divmod(k % (B * Hkv), Hkv)
+            return oracle_part(case, [b], [(b, g)]), N / Hkv
+        b = k % B
+        return oracle_part(case, [b], [(b, g) for g in range(Hkv)]), float(N)
+
+    for k in range(args.warmup):
+        step(k)
     w0 = time.time()
-    v, t, desc, n = time_oracle(case, budget_s=0, steps=args.steps)
+    ts, toks = [], 0.0
+    for k in range(args.steps):
+        t, n = step(args.warmup + k)
+        ts.append(t)
+        toks += n
     wall = time.time() - w0
+    ms = 1e3 * sum(ts) / len(ts)
+    v = toks / sum(ts)
+    desc = ("one (sequence, kv-head) unit of attention plus its sequence's ancestry, argmax rows and walk per "
+            f"step, credited as N/Hkv = {N / Hkv:g} tokens" if per_unit else
+            f"one whole sequence per step ({N} tree tokens: ancestry, attention over all {Hkv} kv heads, argmax of "
+            "its rows, walk)")
     line = {
         "metric": "tree-verify step: tree tokens verified/s", "value": v, "unit": "tree tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
         "config": {"workload": f"{args.workload}: " + WORKLOAD_DESC[args.workload]},
         "cpu_baseline": {"kind": "oracle", "cores": blas_threads(), "value": v,
-                         "sample": f"{desc}; median of {n} steps; {wall:.1f} s wall"},
+                         "sample": f"{desc}; {args.steps} steps in {wall:.1f} s wall, no extrapolation"},
         "e2e": {"value": v, "unit": "tree tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -881,13 +995,20 @@ def default_steps(workload: str) -> int:
     return {"c1": 20000, "c2": 20000, "c3": 2000, "c4": 200, "c5": 200}[workload]
 
 
+DEFAULT_WORKLOAD = "c4"
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="c2")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default=DEFAULT_WORKLOAD,
+                    help="the headline workload (default c4, the largest; the 70B-shaped layer)")
+    ap.add_argument("--sub", default=None,
+                    help="comma-separated workloads measured as sub-records of the same line "
+                         "(default with c4: c3,c5,c2,c1; otherwise none; 'none' for none)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch of c4 (smaller profiling case)")
@@ -901,6 +1022,13 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.sub is None:
+        args.sub = "c3,c5,c2,c1" if (args.workload == DEFAULT_WORKLOAD and args.part == "step" and not args.batch
+                                     and not args.prefix and not args.forest) else "none"
+    args.sub = [] if args.sub in ("", "none") else [w.strip() for w in args.sub.split(",")]
+    for w in args.sub:
+        if w not in WORKLOAD_DESC:
+            raise SystemExit(f"unknown workload in --sub: {w}")
     if args.steps <= 0:
         args.steps = default_steps(args.workload) if args.impl == "ours" else 3
         if args.impl == "ours" and args.part in ("stochastic", "dynamic"):
