@@ -12,41 +12,57 @@
 // also runs the tree block: the N tree keys, gated per row by the ancestry
 // bitmask.  All of these share one online softmax.
 //
-//   warps 0-3  softmax: thread t owns TMEM lane t = row t.  Loads S from TMEM,
+//   warp 0     TMEM allocation; TMA loads of the Q tile and of the K tiles
+//   warp 3     TMA loads of the V tiles (paged blocks: one box per block); K
+//              and V each stream through their own ring.  At CTA start it
+//              also prefetches the tensor maps, the Q tile and the first
+//              block-table entry into L2, ahead of the launch wait.
+//   warp 1     QK issuer (one thread): S(j) = Q K(j)^T, both operands in
+//              swizzled shared memory, into S buffer j%3 once PV(j-3) (the
+//              last reader of that buffer) has completed (s_free[j%3]).
+//   warp 2     PV issuer (one thread): O += P(j) V(j), P read from TMEM, V
+//              from shared memory, as soon as the softmax has written P(j).
+//   warps 4-7  softmax: thread t owns TMEM lane t = row t.  Loads S from TMEM,
 //              masks, tracks the running max/sum, writes P (bf16) back over S,
 //              rescales O when the max moves by more than 2^20 (exact: the final
 //              normalisation uses the same running max).  At the end each
 //              thread normalises its row of O to bf16 in the idle K ring, in
 //              the 128-byte-swizzled layout of a TMA box, and one thread
 //              stores the boxes: the output itself, or this split's partial.
-//   warp 4     TMEM allocation; TMA loads of the Q tile and of the K tiles
-//   warp 7     TMA loads of the V tiles (paged blocks: one box per block); K
-//              and V each stream through their own 3-stage ring.  At CTA
-//              start it also prefetches the tensor maps, the Q tile and the
-//              first block-table entry into L2, ahead of the launch wait.
-//   warp 5     QK issuer (one thread): S(j) = Q K(j)^T, both operands in
-//              swizzled shared memory, into S buffer j%3 once PV(j-3) (the
-//              last reader of that buffer) has completed (s_free[j%3]).
-//   warp 6     PV issuer (one thread): O += P(j) V(j), P read from TMEM, V
-//              from shared memory, as soon as the softmax has written P(j).
-//   One thread issues a tcgen05.mma only every ~120-160 cycles, about half
-//   the tensor pipe's rate for 128x128x16 instructions; with QK and PV on two
-//   issuers the next tile's QK^T and this tile's PV run while the softmax
-//   works, and the pipe sees both streams at once.
+//   With QK and PV on two issuers the next tile's QK^T and this tile's PV
+//   run while the softmax works.  The control warps are numbered first so
+//   that the scheduler, which favours older warps, serves them before the
+//   issue-bound softmax warp of the same sub-partition.
+//
+// CTA pairs (PAIR, head_dim 128, an even number of row tiles).  The two row
+// tiles 2p and 2p+1 of a unit and split run as one 2-CTA cluster on two SMs
+// and share every K/V tile: each CTA loads half of it (K: 64 of the 128 keys,
+// all D columns; V: all 128 keys, 64 of the D columns), so each SM pulls half
+// the bytes per tile from L2 and the rings are six tiles deep in the same
+// shared memory.  The even CTA issues cta_group::2 MMAs of M = 256 rows for
+// both (its rows and TMEM lanes first): S = Q K^T takes the keys from both
+// CTAs' halves, O += P V takes P from each CTA's own TMEM and the D columns
+// from both.  Its commits arrive on the barriers of both CTAs.  The odd CTA
+// runs its own softmax and producers; two of its threads forward the
+// completion of its own loads (Q, K, V) to the even CTA's barriers, so every
+// load is observed by a barrier of the CTA that issued it, and the even
+// CTA's PV issuer publishes the PV count into the odd CTA's shared memory.
 //
 // Shared-memory K/V tiles of the prefix are laid out [8-row group][D half]
 // [8 rows x 128 B] (each 1 KB piece one 128-byte-swizzle atom), so one TMA box
-// brings every D column of a paged block; tree tiles are [D half][128 rows].
-// TMEM (512 columns): O at [0, D), three S buffers at [128, 256), [256, 384)
-// and [384, 512): QK can run two tiles ahead of the softmax, so the softmax
-// does not wait for the PV that frees the buffer it needs next.
-// The tree block rides on the last prefix split of a unit or, when the host
-// plans it so, on a split of its own that runs beside the prefix splits.
-// Every mbarrier wait is bounded; a timeout sets a shared abort flag and every
-// role winds down.  Before the CTA frees its TMEM and exits, an aborted CTA
-// drains what it still has in flight: the producers wait (bounded) for the
-// loads they issued to land, and each MMA issuer commits to a barrier of its
-// own and waits for its MMAs to finish.  It then reports TS_ERR_TIMEOUT.
+// brings every D column of a paged block (its own D half, for V in a pair);
+// tree tiles are [D half][rows].  TMEM (512 columns): O at [0, D), three S
+// buffers at [128, 256), [256, 384) and [384, 512): QK can run two tiles ahead
+// of the softmax, so the softmax does not wait for the PV that frees the
+// buffer it needs next.  The tree block rides on the last prefix split of a
+// unit or, when the host plans it so, on a split of its own that runs beside
+// the prefix splits.
+// Every mbarrier wait is bounded; a timeout sets an abort flag (in a pair,
+// both CTAs' flags) and every role winds down.  Before the CTA frees its TMEM
+// and exits, an aborted CTA drains what it still has in flight: the producers
+// wait (bounded) for the loads they issued to land, and each MMA issuer
+// commits to a barrier of its own and waits for its MMAs to finish.  It then
+// reports TS_ERR_TIMEOUT.
 #include "fastexp.cuh"
 #include "internal.cuh"
 #include "sm100.cuh"
@@ -59,10 +75,16 @@ using namespace sm100;
 
 constexpr int NUM_THREADS = 256;
 constexpr int SOFTMAX_THREADS = 128;
-constexpr int PRODUCER_WARP = 4;
-constexpr int QK_WARP = 5;
-constexpr int PV_WARP = 6;
-constexpr int V_PRODUCER_WARP = 7;
+// The control warps come first: on each SM sub-partition a control warp
+// shares the issue slots with one softmax warp, and the scheduler favours the
+// older (lower-numbered) warp.  With the softmax first, the producers and MMA
+// issuers were measured to run at ~15-20 cycles per instruction (8 TMA boxes
+// or 8 MMAs of a tile took ~700 cycles to issue) and set the tile period.
+constexpr int PRODUCER_WARP = 0;
+constexpr int QK_WARP = 1;
+constexpr int PV_WARP = 2;
+constexpr int V_PRODUCER_WARP = 3;
+constexpr int SOFTMAX_WARP0 = 4;  // warps 4-7; warp w reads TMEM lanes 32 * (w % 4) ..
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_O = 0;
 constexpr uint32_t TMEM_S0 = 128;
@@ -76,25 +98,30 @@ constexpr int NSB = 3;  // S buffers in TMEM
 constexpr float RESCALE_THRESHOLD = 20.0f;
 constexpr float NEG_INF = -INFINITY;
 
-template <int D>
+template <int D, bool PAIR>
 struct Cfg {
   static constexpr int HALVES = D / 64;                        // 128-byte swizzle atoms along D
-  static constexpr int TILE_BYTES = KV_TILE * D * 2;           // one K or V tile
-  static constexpr int HALF_BYTES = KV_TILE * 128;             // one 64-column half of a tile
+  static constexpr int K_KEYS = PAIR ? KV_TILE / 2 : KV_TILE;  // keys of a K tile this CTA holds
+  static constexpr int V_HALVES = PAIR ? 1 : HALVES;           // D halves of a V tile this CTA holds
+  static constexpr int K_TILE_BYTES = K_KEYS * D * 2;
+  static constexpr int V_TILE_BYTES = KV_TILE * 128 * V_HALVES;
+  static constexpr int K_TREE_HALF = K_KEYS * 128;             // one D half of a tree K tile
+  static constexpr int V_TREE_HALF = KV_TILE * 128;            // one D half of a tree V tile
   static constexpr int Q_BYTES = ROW_TILE * D * 2;
-  static constexpr int NST = (D == 128) ? 3 : 6;               // K/V ring depth
+  static constexpr int NST = PAIR ? 6 : ((D == 128) ? 3 : 6);  // K/V ring depth
 };
 
-template <int D>
+template <int D, bool PAIR>
 struct __align__(1024) Smem {
-  uint8_t q[Cfg<D>::Q_BYTES];
-  uint8_t k[Cfg<D>::NST][Cfg<D>::TILE_BYTES];
-  uint8_t v[Cfg<D>::NST][Cfg<D>::TILE_BYTES];
+  using C = Cfg<D, PAIR>;
+  uint8_t q[C::Q_BYTES];
+  uint8_t k[C::NST][C::K_TILE_BYTES];
+  uint8_t v[C::NST][C::V_TILE_BYTES];
   uint64_t q_full;
-  uint64_t k_full[Cfg<D>::NST];
-  uint64_t v_full[Cfg<D>::NST];
-  uint64_t k_empty[Cfg<D>::NST];  // K slot free: its QK completed
-  uint64_t v_empty[Cfg<D>::NST];  // V slot free: its PV completed
+  uint64_t k_full[C::NST];
+  uint64_t v_full[C::NST];
+  uint64_t k_empty[C::NST];  // K slot free: its QK completed
+  uint64_t v_empty[C::NST];  // V slot free: its PV completed
   uint64_t s_full[NSB];
   uint64_t p_full[NSB];
   uint64_t s_free[NSB];  // S buffer b no longer read: PV of its last tile completed
@@ -103,43 +130,66 @@ struct __align__(1024) Smem {
   uint32_t tmem_base;
   int abort_flag;
   int pv_done;  // PVs completed so far, published by the PV issuer (release/acquire)
+  int fwd[3];   // pair, even CTA: Q / K / V loads of the odd CTA forwarded so far (final at teardown)
 };
 
 struct TcArgs {
   AttnArgs a;
   int box_rows;   // rows per paged TMA box: min(block_size, 128)
+  int kbox_rows;  // pair: rows per paged K box, min(block_size, 64)
   int direct;     // 1: a single split per unit -> write bf16 out (+ lse) directly
 };
 
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit) {
+// Abort state of a CTA: its own flag, the wait limit, and in a pair the
+// shared::cluster address of the peer's flag (0 when there is no peer).
+struct Ctl {
+  volatile int* flag;
+  uint64_t limit;
+  uint32_t peer_flag;
+};
+
+__device__ __forceinline__ void raise_abort(const Ctl& c) {
+  *c.flag = 1;
+  if (c.peer_flag) st_cluster_u32(c.peer_flag, 1u);
+}
+
+// Bounded wait that also gives up as soon as another role (or the peer CTA)
+// has aborted.  CTA-scope acquire: a cluster-scope one costs a fence per
+// wait, which on the softmax's per-tile wait was measured to cost a third
+// of the pair's throughput.  Every cross-CTA hand-off in a pair carries data
+// that is complete in shared or tensor memory before its arrive is issued.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > limit) {
-      *abort_flag = 1;
+    if (*c.flag) return false;
+    if (globaltimer_ns() - t0 > c.limit) {
+      raise_abort(c);
       return false;
     }
   }
 }
 
 // Bounded wait until the published PV count reaches `target`.
-__device__ __forceinline__ bool wait_count(const int* counter, int target, volatile int* abort_flag, uint64_t limit) {
+template <bool CL>
+__device__ __forceinline__ bool wait_count(const int* counter, int target, const Ctl& c) {
   const uint32_t addr = smem_u32(counter);
   auto load = [&]() {
     int v;
-    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    if (CL)
+      asm volatile("ld.acquire.cluster.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    else
+      asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
   };
   if (load() >= target) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (load() >= target) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > limit) {
-      *abort_flag = 1;
+    if (*c.flag) return false;
+    if (globaltimer_ns() - t0 > c.limit) {
+      raise_abort(c);
       return false;
     }
   }
@@ -158,25 +208,35 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int D>
+template <int D, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tm_q,
           const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
           const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
           const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_po) {
-  using C = Cfg<D>;
+  using C = Cfg<D, PAIR>;
   extern __shared__ uint8_t smem_raw[];
-  Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<D, PAIR>& sm =
+      *reinterpret_cast<Smem<D, PAIR>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const AttnArgs& a = args.a;
   volatile int* abort_flag = &sm.abort_flag;
-  const uint64_t limit = a.wait_limit_ns;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rt = blockIdx.x, split = blockIdx.y, unit = blockIdx.z;
   const int b = unit / a.Hkv, g = unit - b * a.Hkv;
   const int t_begin = split * a.chunk_tiles;
-  const int boxes = KV_TILE / args.box_rows;  // boxes (paged blocks) per tile (1 .. 8)
-  const int tpg = 32 / boxes;                 // tiles per group of block-table entries
+  // pair: rank 0 (the even row tile) issues the MMAs for both CTAs
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const Ctl ctl{abort_flag, a.wait_limit_ns, PAIR ? mapa(smem_u32(&sm.abort_flag), crank ^ 1u) : 0u};
+  // Geometry of this warp's paged loads (producer warps): rows per box,
+  // boxes per tile, tiles per group of 32 block-table entries, first key's
+  // offset in the tile.
+  const bool v_warp = warp == V_PRODUCER_WARP;
+  const int g_box = (PAIR && !v_warp) ? args.kbox_rows : args.box_rows;
+  const int g_boxes = ((PAIR && !v_warp) ? C::K_KEYS : KV_TILE) / g_box;  // 1 .. 8
+  const int g_tpg = 32 / g_boxes;
+  const int g_off = (PAIR && !v_warp) ? C::K_KEYS * (int)crank : 0;
   const int* table_row = a.block_table + (size_t)b * a.max_blocks;
   // First of all, by a warp that has no part in the set-up: fetch the tensor
   // maps (kernel parameters) and prefetch into L2 the Q tile and the
@@ -201,16 +261,20 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
     sm.pv_done = 0;
-    mbar_init(&sm.q_full, 1);
+    sm.fwd[0] = sm.fwd[1] = sm.fwd[2] = 0;
+    // pair, even CTA: a load barrier also counts the odd CTA's forwarded
+    // arrival, and P(j) arrives once per softmax warp of both CTAs
+    const uint32_t fulls = (PAIR && leader) ? 2 : 1;
+    mbar_init(&sm.q_full, fulls);
     for (int i = 0; i < C::NST; ++i) {
-      mbar_init(&sm.k_full[i], 1);
-      mbar_init(&sm.v_full[i], 1);
+      mbar_init(&sm.k_full[i], fulls);
+      mbar_init(&sm.v_full[i], fulls);
       mbar_init(&sm.k_empty[i], 1);
       mbar_init(&sm.v_empty[i], 1);
     }
     for (int i = 0; i < NSB; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.p_full[i], SOFTMAX_THREADS);
+      mbar_init(&sm.p_full[i], PAIR ? 2 * SOFTMAX_THREADS / 32 : SOFTMAX_THREADS);
       mbar_init(&sm.s_free[i], 1);
     }
     mbar_init(&sm.o_ready, 1);
@@ -218,9 +282,16 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     mbar_init(&sm.drain[1], 1);
     fence_barrier_init();
   }
-  if (warp == PRODUCER_WARP) tmem_alloc(&sm.tmem_base, TMEM_COLS);
+  if (warp == PRODUCER_WARP) {
+    if constexpr (PAIR)
+      tmem_alloc_pair(&sm.tmem_base, TMEM_COLS);
+    else
+      tmem_alloc(&sm.tmem_base, TMEM_COLS);
+  }
   tc_fence_before();
   __syncthreads();
+  // a pair: the peer's barriers are initialised before any arrival reaches them
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
@@ -238,7 +309,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   const bool producer = (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && a.max_blocks > 0;
   const int* blk_addr = table_row;
   if (producer) {
-    const long long t0 = (long long)(t_begin + lane / boxes) * KV_TILE + (lane % boxes) * args.box_rows;
+    const long long t0 = (long long)(t_begin + lane / g_boxes) * KV_TILE + g_off + (lane % g_boxes) * g_box;
     const long long idx = t0 / a.bs;
     blk_addr = table_row + (idx < a.max_blocks ? idx : a.max_blocks - 1);
   }
@@ -266,59 +337,120 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     const CUtensorMap* tm_node = is_v ? &tm_vt : &tm_kt;
     uint64_t* full = is_v ? sm.v_full : sm.k_full;
     uint64_t* empty = is_v ? sm.v_empty : sm.k_empty;
-    const uint32_t box_bytes = args.box_rows * D * 2;
+    const uint32_t box_bytes = g_box * (is_v ? C::V_HALVES * 64 : D) * 2;
+    const int half = (PAIR && is_v) ? (int)crank : 0;  // pair: the V box of this CTA's D half
+    // This warp's loop is on the tile period's critical path and shares its
+    // sub-partition with a softmax warp: it was measured to take ~900 cycles
+    // a tile for ~150 dependent integer instructions (runtime divisions, a
+    // 32-lane wait and vote).  So every per-tile quantity is kept
+    // incrementally (boxes per tile and tiles per table group are powers of
+    // two), only lane 0 waits, and a block id is checked when it is used,
+    // not when it is loaded.
+    const int lg_boxes = __ffs(g_boxes) - 1;
+    const int koff = g_off + (lane & (g_boxes - 1)) * g_box;  // this lane's box: keys [koff, +box) of a tile
     // Block-table entries are software-pipelined: lane L holds the entry of
     // box (L % boxes) of tile (L / boxes) of a group of 32/boxes tiles; the
     // next group is loaded (one coalesced read) when the current one starts,
     // so the table's load latency hides behind several tiles of TMA issue.
     auto load_group = [&](int grp) -> int {
-      const int tile = grp * tpg + lane / boxes;
-      const int t0 = (t_begin + tile) * KV_TILE + (lane % boxes) * args.box_rows;
+      const int tile = grp * g_tpg + (lane >> lg_boxes);
+      const int t0 = (t_begin + tile) * KV_TILE + koff;
       if (tile >= n_prefix || t0 >= P) return 0;
-      int blk = grp == 0 ? blk_first : table_row[t0 / a.bs];
-      if (blk < 0 || blk >= a.num_blocks) {
-        if (a.status) a.status[b] = TS_ERR_BAD_BLOCK;
-        blk = 0;  // read a valid block instead; the sequence is reported as failed
-      }
-      return blk;
+      return grp == 0 ? blk_first : table_row[t0 / a.bs];
     };
     int grp_cur = load_group(0);
-    int grp_nxt = (n_prefix > tpg) ? load_group(1) : 0;
+    int grp_nxt = (n_prefix > g_tpg) ? load_group(1) : 0;
     const int stop = (!is_v && b == a.stall_seq) ? a.stall_tile : n_tiles;
+    // key of this lane's box in the current tile, and its row in its block
+    // (constant when blocks divide a tile; else advanced by a tile each step)
+    int key = t_begin * KV_TILE + koff;
+    int row = a.bs <= KV_TILE ? (koff & (a.bs - 1)) : (key % a.bs);
+    int slot = 0, phase = 0, jt = 0;  // ring slot and its phase; tile within the table group
     int j = 0;
     for (; j < n_tiles; ++j) {
-      const int slot = j % C::NST;
       uint8_t* dst = is_v ? sm.v[slot] : sm.k[slot];
-      if (j >= C::NST && !__all_sync(0xffffffffu, wait_bar(&empty[slot], ((j / C::NST) - 1) & 1, abort_flag, limit)))
-        break;
+      if (j >= C::NST) {
+        bool ok = true;
+        if (lane == 0) ok = wait_bar(&empty[slot], phase ^ 1, ctl);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
       if (j == stop) break;
       if (j < n_prefix) {
-        if (j > 0 && j % tpg == 0) {
+        if (jt == 0 && j > 0) {
           grp_cur = grp_nxt;
-          const int g2 = j / tpg + 1;
-          grp_nxt = (g2 * tpg < n_prefix) ? load_group(g2) : 0;
+          const int g2 = (j >> (5 - lg_boxes)) + 1;
+          grp_nxt = (g2 * g_tpg < n_prefix) ? load_group(g2) : 0;
         }
-        const int key0 = (t_begin + j) * KV_TILE;
-        // lane i < boxes handles the box of tokens [key0 + i*box_rows, +box_rows)
-        const int blk = __shfl_sync(0xffffffffu, grp_cur, ((j % tpg) * boxes + lane) & 31);
-        const int t0 = key0 + lane * args.box_rows;
-        const bool issue = lane < boxes && t0 < P;
-        const int row0 = t0 % a.bs;
+        // lane i < boxes handles the box of tokens [key, key + box_rows)
+        int blk = __shfl_sync(0xffffffffu, grp_cur, (jt << lg_boxes) + lane);
+        const bool issue = lane < g_boxes && key < P;
+        if (issue && (blk < 0 || blk >= a.num_blocks)) {
+          if (a.status) a.status[b] = TS_ERR_BAD_BLOCK;
+          blk = 0;  // read a valid block instead; the sequence is reported as failed
+        }
         const unsigned mask = __ballot_sync(0xffffffffu, issue);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], __popc(mask) * box_bytes);
         __syncwarp();
-        // one box = every D column of box_rows tokens of one paged block
-        if (issue) tma_load_5d(dst + lane * box_bytes, tm_pool, &full[slot], 0, 0, 0, row0 >> 3, blk * a.Hkv + g);
+        // one box = every D column (its D half, for V in a pair) of box_rows
+        // tokens of one paged block
+        if (issue) tma_load_5d(dst + lane * box_bytes, tm_pool, &full[slot], 0, 0, half, row >> 3, blk * a.Hkv + g);
+        key += KV_TILE;
+        if (a.bs > KV_TILE) {
+          row += KV_TILE;
+          if (row >= a.bs) row -= a.bs;
+        }
+        jt = (jt + 1) & (g_tpg - 1);
       } else if (lane == 0) {
         const int n0 = (j - n_prefix) * KV_TILE;  // first tree node of this tile; nodes >= N read as zeros
-        mbar_arrive_expect_tx(&full[slot], C::TILE_BYTES);
-        for (int h = 0; h < C::HALVES; ++h) tma_load_4d(dst + h * C::HALF_BYTES, tm_node, &full[slot], 64 * h, g, n0, b);
+        if constexpr (!PAIR) {
+          mbar_arrive_expect_tx(&full[slot], C::K_TILE_BYTES);
+          for (int h = 0; h < C::HALVES; ++h)
+            tma_load_4d(dst + h * C::V_TREE_HALF, tm_node, &full[slot], 64 * h, g, n0, b);
+        } else if (!is_v) {
+          // this CTA's 64 of the tile's 128 nodes, every D column
+          mbar_arrive_expect_tx(&full[slot], C::K_TILE_BYTES);
+          for (int h = 0; h < C::HALVES; ++h)
+            tma_load_4d(dst + h * C::K_TREE_HALF, tm_node, &full[slot], 64 * h, g, n0 + C::K_KEYS * (int)crank, b);
+        } else {
+          // all 128 nodes, this CTA's D half
+          mbar_arrive_expect_tx(&full[slot], C::V_TILE_BYTES);
+          tma_load_4d(dst, tm_node, &full[slot], 64 * (int)crank, g, n0, b);
+        }
       }
       __syncwarp();
+      if (++slot == C::NST) {
+        slot = 0;
+        phase ^= 1;
+      }
     }
     return j;
   };
   int issued = 0;  // tiles this warp's producer issued (K or V), for the drain of an aborted CTA
+
+  // Pair, odd CTA: forward the completion of this CTA's own loads (Q, then
+  // K or V tile by tile) to the even CTA's barriers, which count them as
+  // their second arrival; record how many were forwarded (read by the even
+  // CTA only after the teardown's cluster barrier).
+  auto forwarder = [&](bool is_v) {
+    uint64_t* full = is_v ? sm.v_full : sm.k_full;
+    int nq = 0, n = 0;
+    bool ok = true;
+    if (!is_v) {
+      ok = wait_bar(&sm.q_full, 0, ctl);
+      if (ok) {
+        mbar_arrive_remote(mapa(smem_u32(&sm.q_full), 0));
+        nq = 1;
+      }
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      ok = wait_bar(&full[j % C::NST], (j / C::NST) & 1, ctl);
+      if (!ok) break;
+      mbar_arrive_remote(mapa(smem_u32(&full[j % C::NST]), 0));
+      n = j + 1;
+    }
+    if (!is_v) st_cluster_u32(mapa(smem_u32(&sm.fwd[0]), 0), (uint32_t)nq);
+    st_cluster_u32(mapa(smem_u32(&sm.fwd[is_v ? 2 : 1]), 0), (uint32_t)n);
+  };
 
   if (!has_work) {
     // nothing to do; fall through to the teardown
@@ -334,68 +466,98 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   } else if (warp == V_PRODUCER_WARP) {
     issued = kv_producer(true);
   } else if (warp == QK_WARP) {
-    // ------------------------------------------------------------ QK issuer
-    if (lane == 0) {
-      constexpr uint32_t ID_QK = idesc_bf16_f32(128, KV_TILE, 0, 0);
+    if (PAIR && !leader) {
+      if (lane == 0) forwarder(false);
+    } else if (lane == 0) {
+      // ---------------------------------------------------------- QK issuer
+      constexpr uint32_t ID_QK = idesc_bf16_f32(PAIR ? 2 * ROW_TILE : ROW_TILE, KV_TILE, 0, 0);
       const uint32_t q_addr = smem_u32(sm.q);
-      bool ok = wait_bar(&sm.q_full, 0, abort_flag, limit);
+      bool ok = wait_bar(&sm.q_full, 0, ctl);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int slot = j % C::NST;
         // K(j) has landed; S buffer j%3 is free once PV(j-3) has completed
         // (a per-buffer barrier: it can never run two completions ahead)
-        ok = wait_bar(&sm.k_full[slot], (j / C::NST) & 1, abort_flag, limit) &&
-             (j < NSB || wait_bar(&sm.s_free[j % NSB], ((j / NSB) - 1) & 1, abort_flag, limit));
+        ok = wait_bar(&sm.k_full[slot], (j / C::NST) & 1, ctl) &&
+             (j < NSB || wait_bar(&sm.s_free[j % NSB], ((j / NSB) - 1) & 1, ctl));
         if (!ok) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm.k[slot]);
         const uint32_t d_tmem = tmem + TMEM_S0 + (j % NSB) * 128;
         // prefix tiles: D halves 1 KB apart, 8-row groups HALVES KB apart;
-        // tree tiles: D halves 16 KB apart, 8-row groups 1 KB apart
+        // tree tiles: D halves a half-tile apart, 8-row groups 1 KB apart
         const bool tree = j >= n_prefix;
-        const uint32_t k_half = tree ? C::HALF_BYTES : 1024;
+        const uint32_t k_half = tree ? C::K_TREE_HALF : 1024;
         const uint32_t k_sbo = tree ? 1024 : C::HALVES * 1024;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (ROW_TILE * 128) + (k & 3) * 32;
           const uint32_t koff = (k >> 2) * k_half + (k & 3) * 32;
-          mma_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + koff, 16, k_sbo), ID_QK,
-                 k > 0);
+          const uint64_t ad = smem_desc_sw128(q_addr + off, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(k_addr + koff, 16, k_sbo);
+          if constexpr (PAIR)
+            mma_ss_pair(d_tmem, ad, bd, ID_QK, k > 0);
+          else
+            mma_ss(d_tmem, ad, bd, ID_QK, k > 0);
         }
-        mma_commit(&sm.s_full[j % NSB]);
-        mma_commit(&sm.k_empty[slot]);  // K(j) no longer read
+        if constexpr (PAIR) {
+          mma_commit_pair(smem_u32(&sm.s_full[j % NSB]));
+          mma_commit_pair(mapa(smem_u32(&sm.s_full[j % NSB]), 1));
+          mma_commit_pair(smem_u32(&sm.k_empty[slot]));  // K(j) no longer read, in either CTA
+          mma_commit_pair(mapa(smem_u32(&sm.k_empty[slot]), 1));
+        } else {
+          mma_commit(&sm.s_full[j % NSB]);
+          mma_commit(&sm.k_empty[slot]);  // K(j) no longer read
+        }
       }
     }
   } else if (warp == PV_WARP) {
-    // ------------------------------------------------------------ PV issuer
-    if (lane == 0) {
-      constexpr uint32_t ID_PV = idesc_bf16_f32(128, D, 0, 1);
+    if (PAIR && !leader) {
+      if (lane == 0) forwarder(true);
+    } else if (lane == 0) {
+      // ---------------------------------------------------------- PV issuer
+      constexpr uint32_t ID_PV = idesc_bf16_f32(PAIR ? 2 * ROW_TILE : ROW_TILE, D, 0, 1);
+      const uint32_t peer_pv_done = PAIR ? mapa(smem_u32(&sm.pv_done), 1) : 0u;
       for (int j = 0; j < n_tiles; ++j) {
         const int slot = j % C::NST;
-        if (!wait_bar(&sm.p_full[j % NSB], (j / NSB) & 1, abort_flag, limit)) break;
-        if (!wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag, limit)) break;
+        if (!wait_bar(&sm.p_full[j % NSB], (j / NSB) & 1, ctl)) break;
+        if (!wait_bar(&sm.v_full[slot], (j / C::NST) & 1, ctl)) break;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sm.v[slot]);
         const uint32_t p_tmem = tmem + TMEM_S0 + (j % NSB) * 128;
         const bool tree = j >= n_prefix;
-        const uint32_t v_lbo = tree ? C::HALF_BYTES : 1024;    // between D halves
-        const uint32_t v_sbo = tree ? 1024 : C::HALVES * 1024;  // between 8-key groups
+        // between D halves / 8-key groups; a pair's CTA holds one D half of V
+        const uint32_t v_lbo = (tree && !PAIR) ? C::V_TREE_HALF : 1024;
+        const uint32_t v_sbo = (tree || PAIR) ? 1024 : C::HALVES * 1024;
 #pragma unroll
-        for (int k = 0; k < KV_TILE / 16; ++k)
-          mma_ts(tmem + TMEM_O, p_tmem + k * 8, smem_desc_sw128(v_addr + k * 2 * v_sbo, v_lbo, v_sbo), ID_PV,
-                 j > 0 || k > 0);
-        mma_commit(&sm.o_ready);
-        mma_commit(&sm.s_free[j % NSB]);
-        mma_commit(&sm.v_empty[slot]);  // V(j) no longer read
+        for (int k = 0; k < KV_TILE / 16; ++k) {
+          const uint64_t bd = smem_desc_sw128(v_addr + k * 2 * v_sbo, v_lbo, v_sbo);
+          if constexpr (PAIR)
+            mma_ts_pair(tmem + TMEM_O, p_tmem + k * 8, bd, ID_PV, j > 0 || k > 0);
+          else
+            mma_ts(tmem + TMEM_O, p_tmem + k * 8, bd, ID_PV, j > 0 || k > 0);
+        }
+        if constexpr (PAIR) {
+          mma_commit_pair(smem_u32(&sm.o_ready));
+          mma_commit_pair(smem_u32(&sm.s_free[j % NSB]));
+          mma_commit_pair(smem_u32(&sm.v_empty[slot]));  // V(j) no longer read, in either CTA
+          mma_commit_pair(mapa(smem_u32(&sm.v_empty[slot]), 1));
+        } else {
+          mma_commit(&sm.o_ready);
+          mma_commit(&sm.s_free[j % NSB]);
+          mma_commit(&sm.v_empty[slot]);  // V(j) no longer read
+        }
         // wait for PV(j) here (every phase in order) and publish the count, so
-        // the softmax looks at O only when it has to rescale it
-        if (!wait_bar(&sm.o_ready, j & 1, abort_flag, limit)) break;
+        // the softmax looks at O only when it has to rescale it (a pair: in
+        // both CTAs; the MMA wrote both CTAs' TMEM)
+        if (!wait_bar(&sm.o_ready, j & 1, ctl)) break;
         tc_fence_after();
         asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.pv_done)), "r"(j + 1) : "memory");
+        if constexpr (PAIR) st_relaxed_cluster_u32(peer_pv_done, (uint32_t)(j + 1));
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = threadIdx.x;  // TMEM lane == packed row within the tile
+    const int r = threadIdx.x - SOFTMAX_WARP0 * 32;  // TMEM lane == packed row within the tile
     const int R = a.N * a.G;
     const int grow = rt * ROW_TILE + r;
     const bool active = grow < R;
@@ -409,11 +571,11 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     } else {
       anc[0] = anc[1] = anc[2] = anc[3] = ~0ull;
     }
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float m_run = NEG_INF, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      if (!__all_sync(0xffffffffu, wait_bar(&sm.s_full[j % NSB], (j / NSB) & 1, abort_flag, limit))) {
+      if (!__all_sync(0xffffffffu, wait_bar(&sm.s_full[j % NSB], (j / NSB) & 1, ctl))) {
         ok = false;
         break;
       }
@@ -504,15 +666,16 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       }
       if (tail_zero_v) {
         // rows >= valid of this V tile hold whatever the pool had past the
-        // prefix (or stale data): zero them so 0 * V can never be NaN
+        // prefix (or stale data): zero them so 0 * V can never be NaN (in a
+        // pair each CTA zeroes its own D half)
         const int slot = j % C::NST;
-        if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[slot], (j / C::NST) & 1, abort_flag, limit))) {
+        if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[slot], (j / C::NST) & 1, ctl))) {
           ok = false;
           break;
         }
         if (r >= valid) {
-          for (int hh = 0; hh < C::HALVES; ++hh) {
-            uint4* row = reinterpret_cast<uint4*>(sm.v[slot] + ((r >> 3) * C::HALVES + hh) * 1024 + (r & 7) * 128);
+          for (int hh = 0; hh < C::V_HALVES; ++hh) {
+            uint4* row = reinterpret_cast<uint4*>(sm.v[slot] + ((r >> 3) * C::V_HALVES + hh) * 1024 + (r & 7) * 128);
 #pragma unroll
             for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
           }
@@ -523,7 +686,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         // O must hold PV(0..j-1) complete before it is rescaled.  TMEM loads
         // and stores are warp-collective: the whole warp rescales its rows
         // together, with factor 1 for rows whose max did not move enough.
-        if (!__all_sync(0xffffffffu, wait_count(&sm.pv_done, j, abort_flag, limit))) {
+        if (!__all_sync(0xffffffffu, wait_count<PAIR>(&sm.pv_done, j, ctl))) {
           ok = false;
           break;
         }
@@ -552,14 +715,25 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       l_run += rowsum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sm.p_full[j % NSB]);
+      if constexpr (PAIR) {
+        // P(j) is announced to the even CTA's PV issuer once per warp
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(&sm.p_full[j % NSB]);
+          else
+            mbar_arrive_remote_cta(mapa(smem_u32(&sm.p_full[j % NSB]), 0));
+        }
+      } else {
+        mbar_arrive(&sm.p_full[j % NSB]);
+      }
     }
     // epilogue: wait for the last PV, normalise, stage the rows in shared
     // memory as TMA boxes (128-byte rows, 16-byte chunk k of row r at
     // k ^ (r % 8): the 128-byte swizzle, and conflict-free for these writes),
     // then one thread stores the boxes.  The K ring is idle by now: every QK
     // has completed before the last PV could start.
-    const bool epi = ok && __all_sync(0xffffffffu, wait_count(&sm.pv_done, n_tiles, abort_flag, limit));
+    const bool epi = ok && __all_sync(0xffffffffu, wait_count<PAIR>(&sm.pv_done, n_tiles, ctl));
     uint8_t* stage = &sm.k[0][0];
     float lse2 = 0.f;
     if (epi) {
@@ -592,7 +766,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     // every softmax thread reaches this barrier, whatever happened above
     const bool all_epi = named_barrier_and(1, SOFTMAX_THREADS, epi);
     if (all_epi) {
-      if (threadIdx.x == 0) {
+      if (r == 0) {
         // rows of nodes >= N fall outside the tensor and are not written
         const int node0 = rt * (ROW_TILE / a.G);
         for (int hh = 0; hh < C::HALVES; ++hh) {
@@ -617,41 +791,65 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
 
   tc_fence_before();
   __syncthreads();
+  // a pair: both CTAs are done with every role (the odd CTA's forward counts
+  // and abort flags are final and visible)
+  if constexpr (PAIR) cluster_sync();
   if (*abort_flag) {
-    // A wait gave up.  Nothing may still write this CTA's shared memory or
-    // TMEM once it exits: wait (bounded, regardless of the flag) for the last
-    // loads each producer issued (only the newest NST tiles of a ring can be
-    // outstanding) and for every MMA each issuer started.
+    // A wait gave up (here or, in a pair, in the peer, which raises both
+    // flags, so both CTAs take this branch).  Nothing may still write this
+    // CTA's shared memory or TMEM once it exits: wait (bounded, regardless of
+    // the flag) for the last loads each producer issued (only the newest NST
+    // tiles of a ring can be outstanding) and for every MMA each issuer
+    // started.  A pair's even CTA counts the odd CTA's forwards as second
+    // arrivals on its load barriers: where a forward never came, it arrives
+    // in its place, so the barrier completes when its own bytes have landed.
     if ((warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && lane == 0) {
-      uint64_t* full = warp == PRODUCER_WARP ? sm.k_full : sm.v_full;
-      if (warp == PRODUCER_WARP && has_work) mbar_wait(&sm.q_full, 0, limit);
-      for (int j = max(0, issued - C::NST); j < issued; ++j) mbar_wait(&full[j % C::NST], (j / C::NST) & 1, limit);
-    } else if ((warp == QK_WARP || warp == PV_WARP) && lane == 0) {
+      const bool is_k = warp == PRODUCER_WARP;
+      uint64_t* full = is_k ? sm.k_full : sm.v_full;
+      const bool sub = PAIR && leader;
+      if (is_k && has_work) {
+        if (sub && sm.fwd[0] == 0) mbar_arrive(&sm.q_full);
+        mbar_wait<PAIR>(&sm.q_full, 0, a.wait_limit_ns);
+      }
+      const int fwd = sub ? sm.fwd[is_k ? 1 : 2] : issued;
+      for (int j = max(0, issued - C::NST); j < issued; ++j) {
+        if (sub && j >= fwd) mbar_arrive(&full[j % C::NST]);
+        mbar_wait<PAIR>(&full[j % C::NST], (j / C::NST) & 1, a.wait_limit_ns);
+      }
+    } else if ((warp == QK_WARP || warp == PV_WARP) && lane == 0 && (!PAIR || leader)) {
       uint64_t* d = &sm.drain[warp - QK_WARP];
-      mma_commit(d);
-      mbar_wait(d, 0, limit);
+      if constexpr (PAIR)
+        mma_commit_pair(smem_u32(d));
+      else
+        mma_commit(d);
+      mbar_wait(d, 0, a.wait_limit_ns);
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();
   }
   pdl_trigger();
   if (sm.abort_flag && threadIdx.x == 0 && a.status) a.status[b] = TS_ERR_TIMEOUT;
   if (warp == PRODUCER_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, TMEM_COLS);
+    else
+      tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
-template <int D>
+template <int D, bool PAIR>
 constexpr size_t smem_bytes() {
-  return sizeof(Smem<D>) + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+  return sizeof(Smem<D, PAIR>) + 1024;  // + alignment slack for the 1024-byte swizzle atoms
 }
 
-template <int D>
+template <int D, bool PAIR>
 cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   TcArgs t{};
   t.a = a;
   t.box_rows = a.bs < KV_TILE ? a.bs : KV_TILE;
+  t.kbox_rows = a.bs < KV_TILE / 2 ? a.bs : KV_TILE / 2;
   t.direct = a.max_splits == 1;
   CUtensorMap m_q, m_kc, m_vc, m_kt, m_vt;
   // q [B, N, Hq, D]: dims (D, Hq, N, B); box (64, G, 128/G, 1) = 128 packed rows
@@ -663,21 +861,26 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   }
   // KV pool [num_blocks, Hkv, bs, D] viewed as (64 columns, 8 rows, D/64 halves,
   // bs/8 row groups, num_blocks*Hkv slabs): a box (64, 8, D/64, box_rows/8, 1)
-  // lands in shared memory as [row group][half][8 rows x 128 B]
+  // lands in shared memory as [row group][half][8 rows x 128 B].  A pair's V
+  // box holds one D half, (64, 8, 1, box_rows/8, 1); its K box at most half
+  // the keys of a tile, (64, 8, D/64, kbox_rows/8, 1).
   {
     const uint64_t dims[5] = {64, 8, (uint64_t)(D / 64), (uint64_t)(a.bs / 8), (uint64_t)a.num_blocks * a.Hkv};
     const uint64_t str[4] = {(uint64_t)D * 2, 128, (uint64_t)8 * D * 2, (uint64_t)a.bs * D * 2};
-    const uint32_t box[5] = {64, 8, (uint32_t)(D / 64), (uint32_t)(t.box_rows / 8), 1};
-    if (!encode_bf16_sw128(&m_kc, a.k_cache, 5, dims, str, box)) return cudaErrorInvalidValue;
-    if (!encode_bf16_sw128(&m_vc, a.v_cache, 5, dims, str, box)) return cudaErrorInvalidValue;
+    const uint32_t kbox[5] = {64, 8, (uint32_t)(D / 64), (uint32_t)((PAIR ? t.kbox_rows : t.box_rows) / 8), 1};
+    const uint32_t vbox[5] = {64, 8, (uint32_t)(PAIR ? 1 : D / 64), (uint32_t)(t.box_rows / 8), 1};
+    if (!encode_bf16_sw128(&m_kc, a.k_cache, 5, dims, str, kbox)) return cudaErrorInvalidValue;
+    if (!encode_bf16_sw128(&m_vc, a.v_cache, 5, dims, str, vbox)) return cudaErrorInvalidValue;
   }
-  // tree K/V [B, N, Hkv, D]: dims (D, Hkv, N, B); box (64, 1, 128, 1); nodes >= N read as zeros
+  // tree K/V [B, N, Hkv, D]: dims (D, Hkv, N, B); box (64, 1, 128, 1); nodes
+  // >= N read as zeros.  A pair's K box holds 64 nodes.
   {
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hkv, (uint64_t)a.N, (uint64_t)a.B};
     const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)a.Hkv * D * 2, (uint64_t)a.N * a.Hkv * D * 2};
-    const uint32_t box[4] = {64, 1, (uint32_t)KV_TILE, 1};
-    if (!encode_bf16_sw128(&m_kt, a.k_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
-    if (!encode_bf16_sw128(&m_vt, a.v_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
+    const uint32_t kbox[4] = {64, 1, (uint32_t)(PAIR ? KV_TILE / 2 : KV_TILE), 1};
+    const uint32_t vbox[4] = {64, 1, (uint32_t)KV_TILE, 1};
+    if (!encode_bf16_sw128(&m_kt, a.k_tree, 4, dims, str, kbox)) return cudaErrorInvalidValue;
+    if (!encode_bf16_sw128(&m_vt, a.v_tree, 4, dims, str, vbox)) return cudaErrorInvalidValue;
   }
   // output boxes of 64 columns: bf16 out [B, N, Hq, D] like q (direct), or the
   // bf16 partial of each split [max_splits, B, N, Hq, D]
@@ -697,8 +900,8 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
     if (!encode_bf16_sw128(&m_po, a.part_o, 5, dims, str, box)) return cudaErrorInvalidValue;
   }
   dim3 grid(a.row_tiles, a.max_splits, a.B * a.Hkv);
-  return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt, m_o,
-                    m_po);
+  return launch_pdl_cluster(k_attn_tc<D, PAIR>, grid, dim3(NUM_THREADS), smem_bytes<D, PAIR>(), s, PAIR ? 2 : 1, t,
+                            m_q, m_kc, m_vc, m_kt, m_vt, m_o, m_po);
 }
 
 }  // namespace
@@ -706,14 +909,19 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
 cudaError_t attn_tc_prepare() {
   // per-process opt-in to the large shared-memory carve-out (not a stream
   // operation; done outside any capture by the first call)
-  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_bytes<128>());
+  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bytes<128, false>());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_attn_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<64>());
+  e = cudaFuncSetAttribute(k_attn_tc<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes<128, true>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_attn_tc<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<64, false>());
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s) {
-  return a.D == 128 ? launch_tc<128>(a, s) : launch_tc<64>(a, s);
+  if (a.D == 128) return a.pair ? launch_tc<128, true>(a, s) : launch_tc<128, false>(a, s);
+  return launch_tc<64, false>(a, s);
 }
 
 }  // namespace ts
