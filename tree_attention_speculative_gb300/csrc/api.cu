@@ -94,12 +94,6 @@ AttnPlan plan_attn(const ts_attn_params* p) {
   }
   pl.chunk_tiles = best_chunk;
   pl.tree_split = best_ts;
-  // The 2-CTA pair variant (row tiles sharing each K/V tile) halves each
-  // SM's K/V traffic but was measured slower than single CTAs on every
-  // workload (c4 attention 944 vs 789 us, c5 1373 vs 1161 us): the tile
-  // period is set by load latency and the softmax, not by L2 or shared-memory
-  // bandwidth, and the pair adds cross-CTA hand-offs.  Single CTAs run.
-  pl.pair = 0;
   pl.max_splits = 1;
   for (int b = 0; b < p->B; ++b) {
     const int ns = num_splits(p->prefix_len_host[b], pl.chunk_tiles, pl.tree_split);
@@ -269,7 +263,6 @@ ts_status attn_fwd_impl(const ts_attn_params* p, void* workspace, size_t workspa
   a.max_splits = pl.max_splits;
   a.tree_split = pl.tree_split;
   a.row_tiles = pl.row_tiles;
-  a.pair = pl.pair;
   a.wait_limit_ns = wait_limit_ns;
   a.stall_seq = stall_seq;
   a.stall_tile = stall_tile;

@@ -30,39 +30,27 @@
 //              the 128-byte-swizzled layout of a TMA box, and one thread
 //              stores the boxes: the output itself, or this split's partial.
 //   With QK and PV on two issuers the next tile's QK^T and this tile's PV
-//   run while the softmax works.  The control warps are numbered first so
-//   that the scheduler, which favours older warps, serves them before the
-//   issue-bound softmax warp of the same sub-partition.
-//
-// CTA pairs (PAIR, head_dim 128, an even number of row tiles).  The two row
-// tiles 2p and 2p+1 of a unit and split run as one 2-CTA cluster on two SMs
-// and share every K/V tile: each CTA loads half of it (K: 64 of the 128 keys,
-// all D columns; V: all 128 keys, 64 of the D columns), so each SM pulls half
-// the bytes per tile from L2 and the rings are six tiles deep in the same
-// shared memory.  The even CTA issues cta_group::2 MMAs of M = 256 rows for
-// both (its rows and TMEM lanes first): S = Q K^T takes the keys from both
-// CTAs' halves, O += P V takes P from each CTA's own TMEM and the D columns
-// from both.  Its commits arrive on the barriers of both CTAs.  The odd CTA
-// runs its own softmax and producers; two of its threads forward the
-// completion of its own loads (Q, K, V) to the even CTA's barriers, so every
-// load is observed by a barrier of the CTA that issued it, and the even
-// CTA's PV issuer publishes the PV count into the odd CTA's shared memory.
+//   run while the softmax works.  Each control warp shares its sub-partition
+//   with a softmax warp, and the scheduler keeps issuing from a ready compute
+//   warp: beside a busy warp a control warp was measured to run several times
+//   slower (8 TMA boxes in ~2500 cycles against ~420 alone), so the producer
+//   loops are kept to a few instructions a tile.  Issuing the loads from the
+//   softmax warps instead was measured slower still (each TMA issue blocks the
+//   issuing warp until the SM's TMA unit, ~50 cycles a 4 KB box, takes it).
 //
 // Shared-memory K/V tiles of the prefix are laid out [8-row group][D half]
 // [8 rows x 128 B] (each 1 KB piece one 128-byte-swizzle atom), so one TMA box
-// brings every D column of a paged block (its own D half, for V in a pair);
-// tree tiles are [D half][rows].  TMEM (512 columns): O at [0, D), three S
-// buffers at [128, 256), [256, 384) and [384, 512): QK can run two tiles ahead
-// of the softmax, so the softmax does not wait for the PV that frees the
-// buffer it needs next.  The tree block rides on the last prefix split of a
-// unit or, when the host plans it so, on a split of its own that runs beside
-// the prefix splits.
-// Every mbarrier wait is bounded; a timeout sets an abort flag (in a pair,
-// both CTAs' flags) and every role winds down.  Before the CTA frees its TMEM
-// and exits, an aborted CTA drains what it still has in flight: the producers
-// wait (bounded) for the loads they issued to land, and each MMA issuer
-// commits to a barrier of its own and waits for its MMAs to finish.  It then
-// reports TS_ERR_TIMEOUT.
+// brings every D column of a paged block; tree tiles are [D half][128 rows].
+// TMEM (512 columns): O at [0, D), three S buffers at [128, 256), [256, 384)
+// and [384, 512): QK can run two tiles ahead of the softmax, so the softmax
+// does not wait for the PV that frees the buffer it needs next.  The tree
+// block rides on the last prefix split of a unit or, when the host plans it
+// so, on a split of its own that runs beside the prefix splits.
+// Every mbarrier wait is bounded; a timeout sets a shared abort flag and every
+// role winds down.  Before the CTA frees its TMEM and exits, an aborted CTA
+// drains what it still has in flight: the producers wait (bounded) for the
+// loads they issued to land, and each MMA issuer commits to a barrier of its
+// own and waits for its MMAs to finish.  It then reports TS_ERR_TIMEOUT.
 #include "fastexp.cuh"
 #include "internal.cuh"
 #include "sm100.cuh"
@@ -75,11 +63,8 @@ using namespace sm100;
 
 constexpr int NUM_THREADS = 256;
 constexpr int SOFTMAX_THREADS = 128;
-// The control warps come first: on each SM sub-partition a control warp
-// shares the issue slots with one softmax warp, and the scheduler favours the
-// older (lower-numbered) warp.  With the softmax first, the producers and MMA
-// issuers were measured to run at ~15-20 cycles per instruction (8 TMA boxes
-// or 8 MMAs of a tile took ~700 cycles to issue) and set the tile period.
+// Warp roles.  On each SM sub-partition one control warp shares the issue
+// slots with one softmax warp (warp w runs on sub-partition w % 4).
 constexpr int PRODUCER_WARP = 0;
 constexpr int QK_WARP = 1;
 constexpr int PV_WARP = 2;
@@ -98,30 +83,29 @@ constexpr int NSB = 3;  // S buffers in TMEM
 constexpr float RESCALE_THRESHOLD = 20.0f;
 constexpr float NEG_INF = -INFINITY;
 
-template <int D, bool PAIR>
+template <int D>
 struct Cfg {
   static constexpr int HALVES = D / 64;                        // 128-byte swizzle atoms along D
-  static constexpr int K_KEYS = PAIR ? KV_TILE / 2 : KV_TILE;  // keys of a K tile this CTA holds
-  static constexpr int V_HALVES = PAIR ? 1 : HALVES;           // D halves of a V tile this CTA holds
-  static constexpr int K_TILE_BYTES = K_KEYS * D * 2;
-  static constexpr int V_TILE_BYTES = KV_TILE * 128 * V_HALVES;
-  static constexpr int K_TREE_HALF = K_KEYS * 128;             // one D half of a tree K tile
-  static constexpr int V_TREE_HALF = KV_TILE * 128;            // one D half of a tree V tile
+  static constexpr int TILE_BYTES = KV_TILE * D * 2;           // one K or V tile
+  static constexpr int HALF_BYTES = KV_TILE * 128;             // one 64-column half of a tile
   static constexpr int Q_BYTES = ROW_TILE * D * 2;
-  static constexpr int NST = PAIR ? 6 : ((D == 128) ? 3 : 6);  // K/V ring depth
+  // Ring depths (K and V), as many tiles as fit beside the Q tile.  Moving a
+  // V slot to K (4 + 2 for D = 128) was measured slower: PV then waited for V.
+  static constexpr int NSTK = (D == 128) ? 3 : 6;
+  static constexpr int NSTV = (D == 128) ? 3 : 6;
 };
 
-template <int D, bool PAIR>
+template <int D>
 struct __align__(1024) Smem {
-  using C = Cfg<D, PAIR>;
+  using C = Cfg<D>;
   uint8_t q[C::Q_BYTES];
-  uint8_t k[C::NST][C::K_TILE_BYTES];
-  uint8_t v[C::NST][C::V_TILE_BYTES];
+  uint8_t k[C::NSTK][C::TILE_BYTES];
+  uint8_t v[C::NSTV][C::TILE_BYTES];
   uint64_t q_full;
-  uint64_t k_full[C::NST];
-  uint64_t v_full[C::NST];
-  uint64_t k_empty[C::NST];  // K slot free: its QK completed
-  uint64_t v_empty[C::NST];  // V slot free: its PV completed
+  uint64_t k_full[C::NSTK];
+  uint64_t v_full[C::NSTV];
+  uint64_t k_empty[C::NSTK];  // K slot free: its QK completed
+  uint64_t v_empty[C::NSTV];  // V slot free: its PV completed
   uint64_t s_full[NSB];
   uint64_t p_full[NSB];
   uint64_t s_free[NSB];  // S buffer b no longer read: PV of its last tile completed
@@ -130,34 +114,21 @@ struct __align__(1024) Smem {
   uint32_t tmem_base;
   int abort_flag;
   int pv_done;  // PVs completed so far, published by the PV issuer (release/acquire)
-  int fwd[3];   // pair, even CTA: Q / K / V loads of the odd CTA forwarded so far (final at teardown)
 };
 
 struct TcArgs {
   AttnArgs a;
   int box_rows;   // rows per paged TMA box: min(block_size, 128)
-  int kbox_rows;  // pair: rows per paged K box, min(block_size, 64)
   int direct;     // 1: a single split per unit -> write bf16 out (+ lse) directly
 };
 
-// Abort state of a CTA: its own flag, the wait limit, and in a pair the
-// shared::cluster address of the peer's flag (0 when there is no peer).
+// Abort state of a CTA: its flag and the wait limit.
 struct Ctl {
   volatile int* flag;
   uint64_t limit;
-  uint32_t peer_flag;
 };
 
-__device__ __forceinline__ void raise_abort(const Ctl& c) {
-  *c.flag = 1;
-  if (c.peer_flag) st_cluster_u32(c.peer_flag, 1u);
-}
-
-// Bounded wait that also gives up as soon as another role (or the peer CTA)
-// has aborted.  CTA-scope acquire: a cluster-scope one costs a fence per
-// wait, which on the softmax's per-tile wait was measured to cost a third
-// of the pair's throughput.  Every cross-CTA hand-off in a pair carries data
-// that is complete in shared or tensor memory before its arrive is issued.
+// Bounded wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -165,22 +136,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const C
     if (mbar_try_wait(bar, parity)) return true;
     if (*c.flag) return false;
     if (globaltimer_ns() - t0 > c.limit) {
-      raise_abort(c);
+      *c.flag = 1;
       return false;
     }
   }
 }
 
 // Bounded wait until the published PV count reaches `target`.
-template <bool CL>
 __device__ __forceinline__ bool wait_count(const int* counter, int target, const Ctl& c) {
   const uint32_t addr = smem_u32(counter);
   auto load = [&]() {
     int v;
-    if (CL)
-      asm volatile("ld.acquire.cluster.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    else
-      asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
   };
   if (load() >= target) return true;
@@ -189,7 +156,7 @@ __device__ __forceinline__ bool wait_count(const int* counter, int target, const
     if (load() >= target) return true;
     if (*c.flag) return false;
     if (globaltimer_ns() - t0 > c.limit) {
-      raise_abort(c);
+      *c.flag = 1;
       return false;
     }
   }
@@ -208,16 +175,15 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int D, bool PAIR>
+template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tm_q,
           const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
           const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
           const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_po) {
-  using C = Cfg<D, PAIR>;
+  using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  Smem<D, PAIR>& sm =
-      *reinterpret_cast<Smem<D, PAIR>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const AttnArgs& a = args.a;
   volatile int* abort_flag = &sm.abort_flag;
 
@@ -225,18 +191,12 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   const int rt = blockIdx.x, split = blockIdx.y, unit = blockIdx.z;
   const int b = unit / a.Hkv, g = unit - b * a.Hkv;
   const int t_begin = split * a.chunk_tiles;
-  // pair: rank 0 (the even row tile) issues the MMAs for both CTAs
-  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
-  const bool leader = crank == 0;
-  const Ctl ctl{abort_flag, a.wait_limit_ns, PAIR ? mapa(smem_u32(&sm.abort_flag), crank ^ 1u) : 0u};
+  const Ctl ctl{abort_flag, a.wait_limit_ns};
   // Geometry of this warp's paged loads (producer warps): rows per box,
-  // boxes per tile, tiles per group of 32 block-table entries, first key's
-  // offset in the tile.
-  const bool v_warp = warp == V_PRODUCER_WARP;
-  const int g_box = (PAIR && !v_warp) ? args.kbox_rows : args.box_rows;
-  const int g_boxes = ((PAIR && !v_warp) ? C::K_KEYS : KV_TILE) / g_box;  // 1 .. 8
+  // boxes per tile, tiles per group of 32 block-table entries.
+  const int g_box = args.box_rows;
+  const int g_boxes = KV_TILE / g_box;  // 1 .. 8
   const int g_tpg = 32 / g_boxes;
-  const int g_off = (PAIR && !v_warp) ? C::K_KEYS * (int)crank : 0;
   const int* table_row = a.block_table + (size_t)b * a.max_blocks;
   // First of all, by a warp that has no part in the set-up: fetch the tensor
   // maps (kernel parameters) and prefetch into L2 the Q tile and the
@@ -261,20 +221,18 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
     sm.pv_done = 0;
-    sm.fwd[0] = sm.fwd[1] = sm.fwd[2] = 0;
-    // pair, even CTA: a load barrier also counts the odd CTA's forwarded
-    // arrival, and P(j) arrives once per softmax warp of both CTAs
-    const uint32_t fulls = (PAIR && leader) ? 2 : 1;
-    mbar_init(&sm.q_full, fulls);
-    for (int i = 0; i < C::NST; ++i) {
-      mbar_init(&sm.k_full[i], fulls);
-      mbar_init(&sm.v_full[i], fulls);
+    mbar_init(&sm.q_full, 1);
+    for (int i = 0; i < C::NSTK; ++i) {
+      mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], 1);
+    }
+    for (int i = 0; i < C::NSTV; ++i) {
+      mbar_init(&sm.v_full[i], 1);
       mbar_init(&sm.v_empty[i], 1);
     }
     for (int i = 0; i < NSB; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.p_full[i], PAIR ? 2 * SOFTMAX_THREADS / 32 : SOFTMAX_THREADS);
+      mbar_init(&sm.p_full[i], SOFTMAX_THREADS);
       mbar_init(&sm.s_free[i], 1);
     }
     mbar_init(&sm.o_ready, 1);
@@ -282,16 +240,9 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     mbar_init(&sm.drain[1], 1);
     fence_barrier_init();
   }
-  if (warp == PRODUCER_WARP) {
-    if constexpr (PAIR)
-      tmem_alloc_pair(&sm.tmem_base, TMEM_COLS);
-    else
-      tmem_alloc(&sm.tmem_base, TMEM_COLS);
-  }
+  if (warp == PRODUCER_WARP) tmem_alloc(&sm.tmem_base, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  // a pair: the peer's barriers are initialised before any arrival reaches them
-  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
@@ -309,7 +260,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   const bool producer = (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && a.max_blocks > 0;
   const int* blk_addr = table_row;
   if (producer) {
-    const long long t0 = (long long)(t_begin + lane / g_boxes) * KV_TILE + g_off + (lane % g_boxes) * g_box;
+    const long long t0 = (long long)(t_begin + lane / g_boxes) * KV_TILE + (lane % g_boxes) * g_box;
     const long long idx = t0 / a.bs;
     blk_addr = table_row + (idx < a.max_blocks ? idx : a.max_blocks - 1);
   }
@@ -337,8 +288,8 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     const CUtensorMap* tm_node = is_v ? &tm_vt : &tm_kt;
     uint64_t* full = is_v ? sm.v_full : sm.k_full;
     uint64_t* empty = is_v ? sm.v_empty : sm.k_empty;
-    const uint32_t box_bytes = g_box * (is_v ? C::V_HALVES * 64 : D) * 2;
-    const int half = (PAIR && is_v) ? (int)crank : 0;  // pair: the V box of this CTA's D half
+    const int nst = is_v ? C::NSTV : C::NSTK;
+    const uint32_t box_bytes = g_box * D * 2;
     // This warp's loop is on the tile period's critical path and shares its
     // sub-partition with a softmax warp: it was measured to take ~900 cycles
     // a tile for ~150 dependent integer instructions (runtime divisions, a
@@ -347,7 +298,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     // two), only lane 0 waits, and a block id is checked when it is used,
     // not when it is loaded.
     const int lg_boxes = __ffs(g_boxes) - 1;
-    const int koff = g_off + (lane & (g_boxes - 1)) * g_box;  // this lane's box: keys [koff, +box) of a tile
+    const int koff = (lane & (g_boxes - 1)) * g_box;  // this lane's box: keys [koff, +box) of a tile
     // Block-table entries are software-pipelined: lane L holds the entry of
     // box (L % boxes) of tile (L / boxes) of a group of 32/boxes tiles; the
     // next group is loaded (one coalesced read) when the current one starts,
@@ -369,7 +320,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     int j = 0;
     for (; j < n_tiles; ++j) {
       uint8_t* dst = is_v ? sm.v[slot] : sm.k[slot];
-      if (j >= C::NST) {
+      if (j >= nst) {
         bool ok = true;
         if (lane == 0) ok = wait_bar(&empty[slot], phase ^ 1, ctl);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -391,9 +342,8 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         const unsigned mask = __ballot_sync(0xffffffffu, issue);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], __popc(mask) * box_bytes);
         __syncwarp();
-        // one box = every D column (its D half, for V in a pair) of box_rows
-        // tokens of one paged block
-        if (issue) tma_load_5d(dst + lane * box_bytes, tm_pool, &full[slot], 0, 0, half, row >> 3, blk * a.Hkv + g);
+        // one box = every D column of box_rows tokens of one paged block
+        if (issue) tma_load_5d(dst + lane * box_bytes, tm_pool, &full[slot], 0, 0, 0, row >> 3, blk * a.Hkv + g);
         key += KV_TILE;
         if (a.bs > KV_TILE) {
           row += KV_TILE;
@@ -402,23 +352,11 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         jt = (jt + 1) & (g_tpg - 1);
       } else if (lane == 0) {
         const int n0 = (j - n_prefix) * KV_TILE;  // first tree node of this tile; nodes >= N read as zeros
-        if constexpr (!PAIR) {
-          mbar_arrive_expect_tx(&full[slot], C::K_TILE_BYTES);
-          for (int h = 0; h < C::HALVES; ++h)
-            tma_load_4d(dst + h * C::V_TREE_HALF, tm_node, &full[slot], 64 * h, g, n0, b);
-        } else if (!is_v) {
-          // this CTA's 64 of the tile's 128 nodes, every D column
-          mbar_arrive_expect_tx(&full[slot], C::K_TILE_BYTES);
-          for (int h = 0; h < C::HALVES; ++h)
-            tma_load_4d(dst + h * C::K_TREE_HALF, tm_node, &full[slot], 64 * h, g, n0 + C::K_KEYS * (int)crank, b);
-        } else {
-          // all 128 nodes, this CTA's D half
-          mbar_arrive_expect_tx(&full[slot], C::V_TILE_BYTES);
-          tma_load_4d(dst, tm_node, &full[slot], 64 * (int)crank, g, n0, b);
-        }
+        mbar_arrive_expect_tx(&full[slot], C::TILE_BYTES);
+        for (int h = 0; h < C::HALVES; ++h) tma_load_4d(dst + h * C::HALF_BYTES, tm_node, &full[slot], 64 * h, g, n0, b);
       }
       __syncwarp();
-      if (++slot == C::NST) {
+      if (++slot == nst) {
         slot = 0;
         phase ^= 1;
       }
@@ -426,31 +364,6 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     return j;
   };
   int issued = 0;  // tiles this warp's producer issued (K or V), for the drain of an aborted CTA
-
-  // Pair, odd CTA: forward the completion of this CTA's own loads (Q, then
-  // K or V tile by tile) to the even CTA's barriers, which count them as
-  // their second arrival; record how many were forwarded (read by the even
-  // CTA only after the teardown's cluster barrier).
-  auto forwarder = [&](bool is_v) {
-    uint64_t* full = is_v ? sm.v_full : sm.k_full;
-    int nq = 0, n = 0;
-    bool ok = true;
-    if (!is_v) {
-      ok = wait_bar(&sm.q_full, 0, ctl);
-      if (ok) {
-        mbar_arrive_remote(mapa(smem_u32(&sm.q_full), 0));
-        nq = 1;
-      }
-    }
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      ok = wait_bar(&full[j % C::NST], (j / C::NST) & 1, ctl);
-      if (!ok) break;
-      mbar_arrive_remote(mapa(smem_u32(&full[j % C::NST]), 0));
-      n = j + 1;
-    }
-    if (!is_v) st_cluster_u32(mapa(smem_u32(&sm.fwd[0]), 0), (uint32_t)nq);
-    st_cluster_u32(mapa(smem_u32(&sm.fwd[is_v ? 2 : 1]), 0), (uint32_t)n);
-  };
 
   if (!has_work) {
     // nothing to do; fall through to the teardown
@@ -466,93 +379,63 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   } else if (warp == V_PRODUCER_WARP) {
     issued = kv_producer(true);
   } else if (warp == QK_WARP) {
-    if (PAIR && !leader) {
-      if (lane == 0) forwarder(false);
-    } else if (lane == 0) {
+    if (lane == 0) {
       // ---------------------------------------------------------- QK issuer
-      constexpr uint32_t ID_QK = idesc_bf16_f32(PAIR ? 2 * ROW_TILE : ROW_TILE, KV_TILE, 0, 0);
+      constexpr uint32_t ID_QK = idesc_bf16_f32(ROW_TILE, KV_TILE, 0, 0);
       const uint32_t q_addr = smem_u32(sm.q);
       bool ok = wait_bar(&sm.q_full, 0, ctl);
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int slot = j % C::NST;
+        const int slot = j % C::NSTK;
         // K(j) has landed; S buffer j%3 is free once PV(j-3) has completed
         // (a per-buffer barrier: it can never run two completions ahead)
-        ok = wait_bar(&sm.k_full[slot], (j / C::NST) & 1, ctl) &&
+        ok = wait_bar(&sm.k_full[slot], (j / C::NSTK) & 1, ctl) &&
              (j < NSB || wait_bar(&sm.s_free[j % NSB], ((j / NSB) - 1) & 1, ctl));
         if (!ok) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm.k[slot]);
         const uint32_t d_tmem = tmem + TMEM_S0 + (j % NSB) * 128;
         // prefix tiles: D halves 1 KB apart, 8-row groups HALVES KB apart;
-        // tree tiles: D halves a half-tile apart, 8-row groups 1 KB apart
+        // tree tiles: D halves 16 KB apart, 8-row groups 1 KB apart
         const bool tree = j >= n_prefix;
-        const uint32_t k_half = tree ? C::K_TREE_HALF : 1024;
+        const uint32_t k_half = tree ? C::HALF_BYTES : 1024;
         const uint32_t k_sbo = tree ? 1024 : C::HALVES * 1024;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (ROW_TILE * 128) + (k & 3) * 32;
           const uint32_t koff = (k >> 2) * k_half + (k & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(q_addr + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(k_addr + koff, 16, k_sbo);
-          if constexpr (PAIR)
-            mma_ss_pair(d_tmem, ad, bd, ID_QK, k > 0);
-          else
-            mma_ss(d_tmem, ad, bd, ID_QK, k > 0);
+          mma_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + koff, 16, k_sbo), ID_QK,
+                 k > 0);
         }
-        if constexpr (PAIR) {
-          mma_commit_pair(smem_u32(&sm.s_full[j % NSB]));
-          mma_commit_pair(mapa(smem_u32(&sm.s_full[j % NSB]), 1));
-          mma_commit_pair(smem_u32(&sm.k_empty[slot]));  // K(j) no longer read, in either CTA
-          mma_commit_pair(mapa(smem_u32(&sm.k_empty[slot]), 1));
-        } else {
-          mma_commit(&sm.s_full[j % NSB]);
-          mma_commit(&sm.k_empty[slot]);  // K(j) no longer read
-        }
+        mma_commit(&sm.s_full[j % NSB]);
+        mma_commit(&sm.k_empty[slot]);  // K(j) no longer read
       }
     }
   } else if (warp == PV_WARP) {
-    if (PAIR && !leader) {
-      if (lane == 0) forwarder(true);
-    } else if (lane == 0) {
+    if (lane == 0) {
       // ---------------------------------------------------------- PV issuer
-      constexpr uint32_t ID_PV = idesc_bf16_f32(PAIR ? 2 * ROW_TILE : ROW_TILE, D, 0, 1);
-      const uint32_t peer_pv_done = PAIR ? mapa(smem_u32(&sm.pv_done), 1) : 0u;
+      constexpr uint32_t ID_PV = idesc_bf16_f32(ROW_TILE, D, 0, 1);
       for (int j = 0; j < n_tiles; ++j) {
-        const int slot = j % C::NST;
+        const int slot = j % C::NSTV;
         if (!wait_bar(&sm.p_full[j % NSB], (j / NSB) & 1, ctl)) break;
-        if (!wait_bar(&sm.v_full[slot], (j / C::NST) & 1, ctl)) break;
+        if (!wait_bar(&sm.v_full[slot], (j / C::NSTV) & 1, ctl)) break;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sm.v[slot]);
         const uint32_t p_tmem = tmem + TMEM_S0 + (j % NSB) * 128;
         const bool tree = j >= n_prefix;
-        // between D halves / 8-key groups; a pair's CTA holds one D half of V
-        const uint32_t v_lbo = (tree && !PAIR) ? C::V_TREE_HALF : 1024;
-        const uint32_t v_sbo = (tree || PAIR) ? 1024 : C::HALVES * 1024;
+        const uint32_t v_lbo = tree ? C::HALF_BYTES : 1024;    // between D halves
+        const uint32_t v_sbo = tree ? 1024 : C::HALVES * 1024;  // between 8-key groups
 #pragma unroll
-        for (int k = 0; k < KV_TILE / 16; ++k) {
-          const uint64_t bd = smem_desc_sw128(v_addr + k * 2 * v_sbo, v_lbo, v_sbo);
-          if constexpr (PAIR)
-            mma_ts_pair(tmem + TMEM_O, p_tmem + k * 8, bd, ID_PV, j > 0 || k > 0);
-          else
-            mma_ts(tmem + TMEM_O, p_tmem + k * 8, bd, ID_PV, j > 0 || k > 0);
-        }
-        if constexpr (PAIR) {
-          mma_commit_pair(smem_u32(&sm.o_ready));
-          mma_commit_pair(smem_u32(&sm.s_free[j % NSB]));
-          mma_commit_pair(smem_u32(&sm.v_empty[slot]));  // V(j) no longer read, in either CTA
-          mma_commit_pair(mapa(smem_u32(&sm.v_empty[slot]), 1));
-        } else {
-          mma_commit(&sm.o_ready);
-          mma_commit(&sm.s_free[j % NSB]);
-          mma_commit(&sm.v_empty[slot]);  // V(j) no longer read
-        }
+        for (int k = 0; k < KV_TILE / 16; ++k)
+          mma_ts(tmem + TMEM_O, p_tmem + k * 8, smem_desc_sw128(v_addr + k * 2 * v_sbo, v_lbo, v_sbo), ID_PV,
+                 j > 0 || k > 0);
+        mma_commit(&sm.o_ready);
+        mma_commit(&sm.s_free[j % NSB]);
+        mma_commit(&sm.v_empty[slot]);  // V(j) no longer read
         // wait for PV(j) here (every phase in order) and publish the count, so
-        // the softmax looks at O only when it has to rescale it (a pair: in
-        // both CTAs; the MMA wrote both CTAs' TMEM)
+        // the softmax looks at O only when it has to rescale it
         if (!wait_bar(&sm.o_ready, j & 1, ctl)) break;
         tc_fence_after();
         asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.pv_done)), "r"(j + 1) : "memory");
-        if constexpr (PAIR) st_relaxed_cluster_u32(peer_pv_done, (uint32_t)(j + 1));
       }
     }
   } else {
@@ -666,16 +549,15 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       }
       if (tail_zero_v) {
         // rows >= valid of this V tile hold whatever the pool had past the
-        // prefix (or stale data): zero them so 0 * V can never be NaN (in a
-        // pair each CTA zeroes its own D half)
-        const int slot = j % C::NST;
-        if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[slot], (j / C::NST) & 1, ctl))) {
+        // prefix (or stale data): zero them so 0 * V can never be NaN
+        const int slot = j % C::NSTV;
+        if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[slot], (j / C::NSTV) & 1, ctl))) {
           ok = false;
           break;
         }
         if (r >= valid) {
-          for (int hh = 0; hh < C::V_HALVES; ++hh) {
-            uint4* row = reinterpret_cast<uint4*>(sm.v[slot] + ((r >> 3) * C::V_HALVES + hh) * 1024 + (r & 7) * 128);
+          for (int hh = 0; hh < C::HALVES; ++hh) {
+            uint4* row = reinterpret_cast<uint4*>(sm.v[slot] + ((r >> 3) * C::HALVES + hh) * 1024 + (r & 7) * 128);
 #pragma unroll
             for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
           }
@@ -686,7 +568,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         // O must hold PV(0..j-1) complete before it is rescaled.  TMEM loads
         // and stores are warp-collective: the whole warp rescales its rows
         // together, with factor 1 for rows whose max did not move enough.
-        if (!__all_sync(0xffffffffu, wait_count<PAIR>(&sm.pv_done, j, ctl))) {
+        if (!__all_sync(0xffffffffu, wait_count(&sm.pv_done, j, ctl))) {
           ok = false;
           break;
         }
@@ -715,25 +597,14 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       l_run += rowsum;
       tmem_st_wait();
       tc_fence_before();
-      if constexpr (PAIR) {
-        // P(j) is announced to the even CTA's PV issuer once per warp
-        __syncwarp();
-        if (lane == 0) {
-          if (leader)
-            mbar_arrive(&sm.p_full[j % NSB]);
-          else
-            mbar_arrive_remote_cta(mapa(smem_u32(&sm.p_full[j % NSB]), 0));
-        }
-      } else {
-        mbar_arrive(&sm.p_full[j % NSB]);
-      }
+      mbar_arrive(&sm.p_full[j % NSB]);
     }
     // epilogue: wait for the last PV, normalise, stage the rows in shared
     // memory as TMA boxes (128-byte rows, 16-byte chunk k of row r at
     // k ^ (r % 8): the 128-byte swizzle, and conflict-free for these writes),
     // then one thread stores the boxes.  The K ring is idle by now: every QK
     // has completed before the last PV could start.
-    const bool epi = ok && __all_sync(0xffffffffu, wait_count<PAIR>(&sm.pv_done, n_tiles, ctl));
+    const bool epi = ok && __all_sync(0xffffffffu, wait_count(&sm.pv_done, n_tiles, ctl));
     uint8_t* stage = &sm.k[0][0];
     float lse2 = 0.f;
     if (epi) {
@@ -791,65 +662,43 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
 
   tc_fence_before();
   __syncthreads();
-  // a pair: both CTAs are done with every role (the odd CTA's forward counts
-  // and abort flags are final and visible)
-  if constexpr (PAIR) cluster_sync();
   if (*abort_flag) {
-    // A wait gave up (here or, in a pair, in the peer, which raises both
-    // flags, so both CTAs take this branch).  Nothing may still write this
-    // CTA's shared memory or TMEM once it exits: wait (bounded, regardless of
-    // the flag) for the last loads each producer issued (only the newest NST
-    // tiles of a ring can be outstanding) and for every MMA each issuer
-    // started.  A pair's even CTA counts the odd CTA's forwards as second
-    // arrivals on its load barriers: where a forward never came, it arrives
-    // in its place, so the barrier completes when its own bytes have landed.
+    // A wait gave up.  Nothing may still write this CTA's shared memory or
+    // TMEM once it exits: wait (bounded, regardless of the flag) for the last
+    // loads each producer issued (only the newest tiles of a ring, as many
+    // as it has slots, can be outstanding) and for every MMA each issuer
+    // started.
     if ((warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && lane == 0) {
-      const bool is_k = warp == PRODUCER_WARP;
-      uint64_t* full = is_k ? sm.k_full : sm.v_full;
-      const bool sub = PAIR && leader;
-      if (is_k && has_work) {
-        if (sub && sm.fwd[0] == 0) mbar_arrive(&sm.q_full);
-        mbar_wait<PAIR>(&sm.q_full, 0, a.wait_limit_ns);
-      }
-      const int fwd = sub ? sm.fwd[is_k ? 1 : 2] : issued;
-      for (int j = max(0, issued - C::NST); j < issued; ++j) {
-        if (sub && j >= fwd) mbar_arrive(&full[j % C::NST]);
-        mbar_wait<PAIR>(&full[j % C::NST], (j / C::NST) & 1, a.wait_limit_ns);
-      }
-    } else if ((warp == QK_WARP || warp == PV_WARP) && lane == 0 && (!PAIR || leader)) {
+      uint64_t* full = warp == PRODUCER_WARP ? sm.k_full : sm.v_full;
+      const int nst = warp == PRODUCER_WARP ? C::NSTK : C::NSTV;
+      if (warp == PRODUCER_WARP && has_work) mbar_wait(&sm.q_full, 0, a.wait_limit_ns);
+      for (int j = max(0, issued - nst); j < issued; ++j) mbar_wait(&full[j % nst], (j / nst) & 1, a.wait_limit_ns);
+    } else if ((warp == QK_WARP || warp == PV_WARP) && lane == 0) {
       uint64_t* d = &sm.drain[warp - QK_WARP];
-      if constexpr (PAIR)
-        mma_commit_pair(smem_u32(d));
-      else
-        mma_commit(d);
+      mma_commit(d);
       mbar_wait(d, 0, a.wait_limit_ns);
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR) cluster_sync();
   }
   pdl_trigger();
   if (sm.abort_flag && threadIdx.x == 0 && a.status) a.status[b] = TS_ERR_TIMEOUT;
   if (warp == PRODUCER_WARP) {
     tc_fence_after();
-    if constexpr (PAIR)
-      tmem_dealloc_pair(tmem, TMEM_COLS);
-    else
-      tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
-template <int D, bool PAIR>
+template <int D>
 constexpr size_t smem_bytes() {
-  return sizeof(Smem<D, PAIR>) + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+  return sizeof(Smem<D>) + 1024;  // + alignment slack for the 1024-byte swizzle atoms
 }
 
-template <int D, bool PAIR>
+template <int D>
 cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   TcArgs t{};
   t.a = a;
   t.box_rows = a.bs < KV_TILE ? a.bs : KV_TILE;
-  t.kbox_rows = a.bs < KV_TILE / 2 ? a.bs : KV_TILE / 2;
   t.direct = a.max_splits == 1;
   CUtensorMap m_q, m_kc, m_vc, m_kt, m_vt;
   // q [B, N, Hq, D]: dims (D, Hq, N, B); box (64, G, 128/G, 1) = 128 packed rows
@@ -861,26 +710,21 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   }
   // KV pool [num_blocks, Hkv, bs, D] viewed as (64 columns, 8 rows, D/64 halves,
   // bs/8 row groups, num_blocks*Hkv slabs): a box (64, 8, D/64, box_rows/8, 1)
-  // lands in shared memory as [row group][half][8 rows x 128 B].  A pair's V
-  // box holds one D half, (64, 8, 1, box_rows/8, 1); its K box at most half
-  // the keys of a tile, (64, 8, D/64, kbox_rows/8, 1).
+  // lands in shared memory as [row group][half][8 rows x 128 B]
   {
     const uint64_t dims[5] = {64, 8, (uint64_t)(D / 64), (uint64_t)(a.bs / 8), (uint64_t)a.num_blocks * a.Hkv};
     const uint64_t str[4] = {(uint64_t)D * 2, 128, (uint64_t)8 * D * 2, (uint64_t)a.bs * D * 2};
-    const uint32_t kbox[5] = {64, 8, (uint32_t)(D / 64), (uint32_t)((PAIR ? t.kbox_rows : t.box_rows) / 8), 1};
-    const uint32_t vbox[5] = {64, 8, (uint32_t)(PAIR ? 1 : D / 64), (uint32_t)(t.box_rows / 8), 1};
-    if (!encode_bf16_sw128(&m_kc, a.k_cache, 5, dims, str, kbox)) return cudaErrorInvalidValue;
-    if (!encode_bf16_sw128(&m_vc, a.v_cache, 5, dims, str, vbox)) return cudaErrorInvalidValue;
+    const uint32_t box[5] = {64, 8, (uint32_t)(D / 64), (uint32_t)(t.box_rows / 8), 1};
+    if (!encode_bf16_sw128(&m_kc, a.k_cache, 5, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_bf16_sw128(&m_vc, a.v_cache, 5, dims, str, box)) return cudaErrorInvalidValue;
   }
-  // tree K/V [B, N, Hkv, D]: dims (D, Hkv, N, B); box (64, 1, 128, 1); nodes
-  // >= N read as zeros.  A pair's K box holds 64 nodes.
+  // tree K/V [B, N, Hkv, D]: dims (D, Hkv, N, B); box (64, 1, 128, 1); nodes >= N read as zeros
   {
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hkv, (uint64_t)a.N, (uint64_t)a.B};
     const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)a.Hkv * D * 2, (uint64_t)a.N * a.Hkv * D * 2};
-    const uint32_t kbox[4] = {64, 1, (uint32_t)(PAIR ? KV_TILE / 2 : KV_TILE), 1};
-    const uint32_t vbox[4] = {64, 1, (uint32_t)KV_TILE, 1};
-    if (!encode_bf16_sw128(&m_kt, a.k_tree, 4, dims, str, kbox)) return cudaErrorInvalidValue;
-    if (!encode_bf16_sw128(&m_vt, a.v_tree, 4, dims, str, vbox)) return cudaErrorInvalidValue;
+    const uint32_t box[4] = {64, 1, (uint32_t)KV_TILE, 1};
+    if (!encode_bf16_sw128(&m_kt, a.k_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_bf16_sw128(&m_vt, a.v_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
   // output boxes of 64 columns: bf16 out [B, N, Hq, D] like q (direct), or the
   // bf16 partial of each split [max_splits, B, N, Hq, D]
@@ -900,8 +744,8 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
     if (!encode_bf16_sw128(&m_po, a.part_o, 5, dims, str, box)) return cudaErrorInvalidValue;
   }
   dim3 grid(a.row_tiles, a.max_splits, a.B * a.Hkv);
-  return launch_pdl_cluster(k_attn_tc<D, PAIR>, grid, dim3(NUM_THREADS), smem_bytes<D, PAIR>(), s, PAIR ? 2 : 1, t,
-                            m_q, m_kc, m_vc, m_kt, m_vt, m_o, m_po);
+  return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt, m_o,
+                    m_po);
 }
 
 }  // namespace
@@ -909,19 +753,14 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
 cudaError_t attn_tc_prepare() {
   // per-process opt-in to the large shared-memory carve-out (not a stream
   // operation; done outside any capture by the first call)
-  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_bytes<128, false>());
+  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bytes<128>());
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_attn_tc<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem_bytes<128, true>());
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_attn_tc<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes<64, false>());
+  return cudaFuncSetAttribute(k_attn_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<64>());
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s) {
-  if (a.D == 128) return a.pair ? launch_tc<128, true>(a, s) : launch_tc<128, false>(a, s);
-  return launch_tc<64, false>(a, s);
+  return a.D == 128 ? launch_tc<128>(a, s) : launch_tc<64>(a, s);
 }
 
 }  // namespace ts

@@ -35,27 +35,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// The same, with thread-block clusters of `cluster_x` CTAs along x (1: none).
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                                      int cluster_x, Args&&... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = cluster_x;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = cluster_x > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
-
 // Prefix keys are processed in tiles of KV_TILE tokens; packed query rows in
 // tiles of ROW_TILE rows (one MMA M extent).
 constexpr int KV_TILE = 128;
@@ -115,7 +94,6 @@ struct AttnArgs {
   int max_splits;    // splits of the longest sequence, the tree's own split included
   int tree_split;    // 1: the tree block is a split of its own
   int row_tiles;     // ceil(N*G / ROW_TILE)
-  int pair;          // 1: row tiles run as 2-CTA clusters sharing each K/V tile (D 128, row_tiles even)
   // Every bounded wait of the attention kernel gives up after wait_limit_ns.
   // Testing the failure path: with stall_seq >= 0, every CTA of that sequence
   // stops its K stream before tile stall_tile (its loads are never issued),
@@ -130,7 +108,6 @@ struct AttnPlan {
   int max_splits;
   int tree_split;
   int row_tiles;
-  int pair;
   size_t part_o_bytes;
   size_t part_lse_bytes;
   size_t workspace_bytes;
