@@ -46,7 +46,7 @@
  *     16-bit brain-float, row-major, densely packed, 16-byte aligned.
  *   - Supported sizes: 1 <= N <= 256 nodes (W = ceil(N/64) <= 4 mask words),
  *     head_dim D in {64, 128}, Hq = G * Hkv with G in {1, 2, 4, 8, 16},
- *     KV block size a multiple of 16 that divides 128 or is a multiple of 128.
+ *     KV block size any positive multiple of 16.
  *     Anything else returns TS_ERR_UNSUPPORTED.
  */
 #ifndef TREESPEC_H_
@@ -119,8 +119,9 @@ TS_API ts_status tree_build_ancestry(const int32_t* parent_idx, const int32_t* p
  *   v_cache     [num_blocks, Hkv, block_size, D] bf16, the paged verified-prefix
  *               KV pool.  Prefix token t of sequence b, KV head g, is row
  *               (t mod block_size) of block block_table[b, t div block_size].
- *               A contiguous cache is the special case block_size = P,
- *               block_table[b] = {b}.
+ *               A contiguous cache is the special case of one block per
+ *               sequence: block_size = P rounded up to a multiple of 16 (rows
+ *               past P_b are never read into the result), block_table[b] = {b}.
  *   block_table [B, max_blocks] int32; only the first ceil(P_b / block_size)
  *               entries of row b are used (other entries of the row may be
  *               read, never followed).

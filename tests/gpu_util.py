@@ -19,6 +19,12 @@ SMALL = [
     ("contiguous_2k", 2, 26, 8, 2, 128, [2048, 2048], 2048, "widths"),
     ("tree_on_last_split", 5, 130, 8, 8, 128, [3000, 2963, 2926, 2889, 2852], 16, "levels"),
     ("one_split_per_unit", 16, 26, 32, 8, 128, [1500 - 37 * i for i in range(16)], 16, "widths"),
+    # block sizes that neither divide a 128-token tile nor are multiples of it
+    ("bs48", 2, 37, 8, 2, 128, [300, 1000], 48, "random"),
+    ("bs144", 1, 40, 16, 2, 128, [700], 144, "levels"),
+    ("bs80_d64", 2, 20, 4, 2, 64, [333, 150], 80, "random"),
+    # a contiguous cache whose prefixes are not multiples of 16: one 304-row block per sequence
+    ("contiguous_300", 2, 26, 8, 2, 128, [300, 290], 304, "widths"),
 ]
 
 ATOL = 1e-2   # |out - ref| <= ATOL + RTOL * |ref| for bf16 attention outputs

@@ -146,7 +146,8 @@ def test_small_parity_cases_cover_every_split_layout(ts):
     (dict(Hq=24, Hkv=8), -4),      # G = 3
     (dict(Hq=30, Hkv=8), -2),      # not a multiple
     (dict(N=257), -4),
-    (dict(bs=48), -4),
+    (dict(bs=40), -4),             # block sizes must be multiples of 16
+    (dict(bs=8), -4),
     (dict(rope_theta=10000.0), -4),
     (dict(misalign=True), -2),
     (dict(neg_prefix=True), -2),

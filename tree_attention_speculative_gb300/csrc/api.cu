@@ -28,7 +28,7 @@ ts_status check_attn(const ts_attn_params* p) {
   if (p->Hq % p->Hkv != 0) return TS_ERR_SHAPE;
   if (!supported_group(p->Hq / p->Hkv)) return TS_ERR_UNSUPPORTED;
   const int bs = p->block_size;
-  if (bs % 16 != 0 || !((KV_TILE % bs == 0) || (bs % KV_TILE == 0))) return TS_ERR_UNSUPPORTED;
+  if (bs % 16 != 0) return TS_ERR_UNSUPPORTED;
   if (p->rope_theta != 0.f) return TS_ERR_UNSUPPORTED;
   if (!(p->scale >= 0.f) || std::isinf(p->scale)) return TS_ERR_SHAPE;
   for (int b = 0; b < p->B; ++b) {

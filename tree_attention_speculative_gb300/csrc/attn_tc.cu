@@ -118,7 +118,7 @@ struct __align__(1024) Smem {
 
 struct TcArgs {
   AttnArgs a;
-  int box_rows;   // rows per paged TMA box: min(block_size, 128)
+  int box_rows;   // rows per paged TMA box: gcd(block_size, 128), so a box never crosses a block
   int direct;     // 1: a single split per unit -> write bf16 out (+ lse) directly
 };
 
@@ -313,9 +313,11 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     int grp_nxt = (n_prefix > g_tpg) ? load_group(1) : 0;
     const int stop = (!is_v && b == a.stall_seq) ? a.stall_tile : n_tiles;
     // key of this lane's box in the current tile, and its row in its block
-    // (constant when blocks divide a tile; else advanced by a tile each step)
+    // (advanced by a tile, 128 mod block_size rows, each step; constant when
+    // blocks divide a tile)
     int key = t_begin * KV_TILE + koff;
-    int row = a.bs <= KV_TILE ? (koff & (a.bs - 1)) : (key % a.bs);
+    int row = key % a.bs;
+    const int row_step = KV_TILE % a.bs;
     int slot = 0, phase = 0, jt = 0;  // ring slot and its phase; tile within the table group
     int j = 0;
     for (; j < n_tiles; ++j) {
@@ -345,10 +347,8 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         // one box = every D column of box_rows tokens of one paged block
         if (issue) tma_load_5d(dst + lane * box_bytes, tm_pool, &full[slot], 0, 0, 0, row >> 3, blk * a.Hkv + g);
         key += KV_TILE;
-        if (a.bs > KV_TILE) {
-          row += KV_TILE;
-          if (row >= a.bs) row -= a.bs;
-        }
+        row += row_step;
+        if (row >= a.bs) row -= a.bs;
         jt = (jt + 1) & (g_tpg - 1);
       } else if (lane == 0) {
         const int n0 = (j - n_prefix) * KV_TILE;  // first tree node of this tile; nodes >= N read as zeros
@@ -698,7 +698,8 @@ template <int D>
 cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   TcArgs t{};
   t.a = a;
-  t.box_rows = a.bs < KV_TILE ? a.bs : KV_TILE;
+  t.box_rows = KV_TILE;  // gcd(block_size, 128): block sizes are multiples of 16
+  while (a.bs % t.box_rows != 0) t.box_rows >>= 1;
   t.direct = a.max_splits == 1;
   CUtensorMap m_q, m_kc, m_vc, m_kt, m_vt;
   // q [B, N, Hq, D]: dims (D, Hq, N, B); box (64, G, 128/G, 1) = 128 packed rows
