@@ -161,8 +161,9 @@ typedef struct ts_attn_params {
 } ts_attn_params;
 
 /*
- * Bytes of device workspace tree_attn_fwd needs for these sizes (split-prefix
- * partial results).  Host-only: launches nothing, safe without a GPU.
+ * Bytes of device workspace tree_attn_fwd needs for these sizes: 256 bytes
+ * for the attention kernel's work-item counter, then the split-prefix
+ * partial results.  Host-only: launches nothing, safe without a GPU.
  * Returns 0 for arguments tree_attn_fwd would reject.
  */
 TS_API size_t tree_attn_workspace_size(const ts_attn_params* p);
@@ -192,12 +193,17 @@ TS_API ts_status tree_attn_plan(const ts_attn_params* p, int32_t* chunk_tiles, i
  *   out[b,i,h] = softmax(scale * q . k) . v over those keys, lse likewise.
  *
  * workspace: device buffer of at least tree_attn_workspace_size(p) bytes,
- * 256-byte aligned, contents need not be initialised; it is scratch for this
- * call only (calls sharing one workspace must be stream-ordered).
+ * 256-byte aligned, ZERO-FILLED before its first use: its first 256 bytes
+ * hold the counter from which the attention kernel's CTAs (one per SM) take
+ * their work items, and every call, a timed-out one included, leaves them
+ * zero again; the rest is scratch for this call only.  Calls sharing one
+ * workspace must be stream-ordered.
  * Returns TS_ERR_NULL / TS_ERR_SHAPE / TS_ERR_UNSUPPORTED / TS_ERR_WORKSPACE /
  * TS_ERR_CUDA; a block id outside the pool sets status[b] = TS_ERR_BAD_BLOCK
  * (block 0 is read in its place), a timed-out internal wait sets
- * TS_ERR_TIMEOUT.
+ * TS_ERR_TIMEOUT for the sequence of every work item (one 128-row tile of
+ * one (sequence, KV head) and one split of its prefix) that the CTA whose
+ * wait ran out had taken and not finished.
  */
 TS_API ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
                         ts_stream stream);
@@ -205,16 +211,18 @@ TS_API ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t 
 /*
  * tree_attn_fwd_stall_test — for testing the failure path only; the pages
  * have no counterpart.  Runs exactly what tree_attn_fwd runs, except that
- * every attention CTA of sequence `stall_seq` stops its key stream before its
- * tile `stall_tile` (128-token tiles, counted from the start of the CTA's
+ * every work item of sequence `stall_seq` stops its key stream before its
+ * tile `stall_tile` (128-token tiles, counted from the start of the item's
  * split; the tree block's tiles come last): those loads are never issued, so
  * the wait for them runs out after `wait_limit_us` microseconds, and every
  * other bounded wait of the call uses the same limit.  A CTA whose wait runs
  * out lets its loads and MMAs in flight finish, frees its tensor memory and
- * sets status[stall_seq] = TS_ERR_TIMEOUT; CTAs with fewer tiles run to the
- * end.  The outputs of that sequence are then unspecified; the other
+ * sets status[b] = TS_ERR_TIMEOUT for the sequence b of every item it had
+ * taken and not finished (stall_seq's among them); items with fewer tiles run
+ * to the end.  The outputs of those sequences are then unspecified; the other
  * sequences' outputs are those of tree_attn_fwd (with a limit far above
- * their run time), and the device stays usable.
+ * their run time), the workspace's counter is back at zero, and the device
+ * stays usable.
  * Returns TS_ERR_SHAPE for stall_seq outside [0, B) or stall_tile < 0,
  * TS_ERR_UNSUPPORTED for wait_limit_us outside [100, 10^6], else as
  * tree_attn_fwd.
@@ -222,6 +230,22 @@ TS_API ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t 
 TS_API ts_status tree_attn_fwd_stall_test(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
                                           int stall_seq, int stall_tile, uint32_t wait_limit_us,
                                           ts_stream stream);
+
+/*
+ * tree_attn_fwd_ctas_test — for testing only; the pages have no counterpart.
+ * tree_attn_fwd runs one attention CTA per SM, each taking work items until
+ * none is left; this call caps the CTAs at `max_ctas` (>= 1), so that small
+ * cases also send many items, empty splits among them, through each CTA.
+ * With stall_seq >= 0 it also stalls that sequence like
+ * tree_attn_fwd_stall_test; with stall_seq == -1 nothing is stalled and
+ * stall_tile is ignored.  Every bounded wait uses wait_limit_us.
+ * Returns TS_ERR_UNSUPPORTED for max_ctas < 1 or wait_limit_us outside
+ * [100, 10^6], TS_ERR_SHAPE for stall_seq outside [-1, B) or (stall_seq >= 0
+ * and stall_tile < 0), else as tree_attn_fwd.
+ */
+TS_API ts_status tree_attn_fwd_ctas_test(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
+                                         int max_ctas, int stall_seq, int stall_tile, uint32_t wait_limit_us,
+                                         ts_stream stream);
 
 /*
  * Bytes of device workspace tree_verify_greedy needs (a packed argmax key per

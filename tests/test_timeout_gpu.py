@@ -51,7 +51,7 @@ def test_attention_wait_runs_out_and_reports_timeout(stall_seq, stall_tile):
     # do reach the withheld tile
     plan = ts.tree_attn_plan(p)
     assert min(plan["chunk_tiles"], -(-int(case.prefix_len[stall_seq]) // 128)) > stall_tile, plan
-    ws = torch.empty(ts.tree_attn_workspace_size(p), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ts.tree_attn_workspace_size(p), dtype=torch.uint8, device="cuda")
     ts.tree_attn_fwd_stall_test(p, ws, stall_seq, stall_tile, 2000)
     torch.cuda.synchronize()     # the call returns by itself: no hang, no fault
     st = step.status.cpu().tolist()
@@ -79,7 +79,7 @@ def test_stall_test_rejects_bad_arguments():
     step = TreeVerifyStep(case.B, case.N, case.Hq, case.Hkv, case.D, case.prefix_len)
     p = step._params(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["prefix_len"], t["k_tree"],
                      t["v_tree"])
-    ws = torch.empty(ts.tree_attn_workspace_size(p), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ts.tree_attn_workspace_size(p), dtype=torch.uint8, device="cuda")
     L = ts.lib()
     import ctypes
     nb = ws.numel()

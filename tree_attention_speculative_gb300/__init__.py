@@ -57,7 +57,7 @@ _LIB: Optional[ctypes.CDLL] = None
 EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_plan", "tree_attn_fwd",
            "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc",
            "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic", "tree_build_ancestry_forest",
-           "tree_verify_greedy_forest", "tree_attn_fwd_stall_test")
+           "tree_verify_greedy_forest", "tree_attn_fwd_stall_test", "tree_attn_fwd_ctas_test")
 
 # TS_VERIFY_NOALLOC_SCRATCH_BYTES of treespec.h
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.tree_attn_fwd.restype = i32
         L.tree_attn_fwd_stall_test.argtypes = [ctypes.POINTER(AttnParams), vp, sz, i32, i32, ctypes.c_uint32, vp]
         L.tree_attn_fwd_stall_test.restype = i32
+        L.tree_attn_fwd_ctas_test.argtypes = [ctypes.POINTER(AttnParams), vp, sz, i32, i32, i32, ctypes.c_uint32, vp]
+        L.tree_attn_fwd_ctas_test.restype = i32
         L.tree_verify_workspace_size.argtypes = [i32, i32, i32]
         L.tree_verify_workspace_size.restype = sz
         L.tree_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -187,6 +189,16 @@ def tree_attn_fwd_stall_test(params: AttnParams, workspace: torch.Tensor, stall_
     _check(lib().tree_attn_fwd_stall_test(ctypes.byref(params), _p(workspace),
                                           workspace.numel() * workspace.element_size(), stall_seq, stall_tile,
                                           wait_limit_us, _s(stream)), "tree_attn_fwd_stall_test")
+
+
+def tree_attn_fwd_ctas_test(params: AttnParams, workspace: torch.Tensor, max_ctas: int, stall_seq: int = -1,
+                            stall_tile: int = 0, wait_limit_us: int = 1000000, stream=None) -> None:
+    """Testing only: tree_attn_fwd on at most ``max_ctas`` CTAs (and, with
+    ``stall_seq >= 0``, that sequence's key stream stopped as in
+    tree_attn_fwd_stall_test)."""
+    _check(lib().tree_attn_fwd_ctas_test(ctypes.byref(params), _p(workspace),
+                                         workspace.numel() * workspace.element_size(), max_ctas, stall_seq,
+                                         stall_tile, wait_limit_us, _s(stream)), "tree_attn_fwd_ctas_test")
 
 
 def tree_verify_workspace_size(B: int, N: int, V: int) -> int:

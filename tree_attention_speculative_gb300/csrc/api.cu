@@ -102,8 +102,8 @@ AttnPlan plan_attn(const ts_attn_params* p) {
   const size_t nrows = (size_t)p->B * p->N * p->Hq;
   pl.part_o_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * p->D * 2) : 0;
   pl.part_lse_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * sizeof(float)) : 0;
-  pl.workspace_bytes = pl.part_o_bytes + pl.part_lse_bytes;
-  if (pl.workspace_bytes == 0) pl.workspace_bytes = 256;  // keep a non-empty workspace contract
+  // the attention kernel's item counter (256 bytes, zero between calls), then the partials
+  pl.workspace_bytes = ATTN_SCHED_BYTES + pl.part_o_bytes + pl.part_lse_bytes;
   return pl;
 }
 
@@ -233,7 +233,7 @@ ts_status tree_attn_plan(const ts_attn_params* p, int32_t* chunk_tiles, int32_t*
 namespace ts {
 namespace {
 ts_status attn_fwd_impl(const ts_attn_params* p, void* workspace, size_t workspace_bytes, ts_stream stream,
-                        int stall_seq, int stall_tile, unsigned long long wait_limit_ns) {
+                        int stall_seq, int stall_tile, unsigned long long wait_limit_ns, int max_ctas) {
   ts_status st = check_attn(p);
   if (st != TS_OK) return st;
   const AttnPlan pl = plan_attn(p);
@@ -252,8 +252,9 @@ ts_status attn_fwd_impl(const ts_attn_params* p, void* workspace, size_t workspa
   a.lse = p->lse;
   a.status = p->status;
   char* ws = static_cast<char*>(workspace);
-  a.part_o = reinterpret_cast<__nv_bfloat16*>(ws);
-  a.part_lse = reinterpret_cast<float*>(ws + pl.part_o_bytes);
+  a.sched = reinterpret_cast<unsigned*>(ws);
+  a.part_o = reinterpret_cast<__nv_bfloat16*>(ws + ATTN_SCHED_BYTES);
+  a.part_lse = reinterpret_cast<float*>(ws + ATTN_SCHED_BYTES + pl.part_o_bytes);
   a.B = p->B; a.N = p->N; a.Hq = p->Hq; a.Hkv = p->Hkv; a.G = p->Hq / p->Hkv; a.D = p->D;
   a.W = ceil_div(p->N, 64);
   a.bs = p->block_size; a.num_blocks = p->num_blocks; a.max_blocks = p->max_blocks;
@@ -266,6 +267,7 @@ ts_status attn_fwd_impl(const ts_attn_params* p, void* workspace, size_t workspa
   a.wait_limit_ns = wait_limit_ns;
   a.stall_seq = stall_seq;
   a.stall_tile = stall_tile;
+  a.max_ctas = max_ctas;
   cudaStream_t s = (cudaStream_t)stream;
   if (prepare_device() != cudaSuccess) return TS_ERR_CUDA;
   if (launch_attn_tc(a, s) != cudaSuccess) return TS_ERR_CUDA;
@@ -280,7 +282,7 @@ extern "C" {
 
 ts_status tree_attn_fwd(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
                         ts_stream stream) {
-  return ts::attn_fwd_impl(p, workspace, workspace_bytes, stream, -1, 0, ATTN_WAIT_LIMIT_NS);
+  return ts::attn_fwd_impl(p, workspace, workspace_bytes, stream, -1, 0, ATTN_WAIT_LIMIT_NS, 0);
 }
 
 ts_status tree_attn_fwd_stall_test(const ts_attn_params* p, void* workspace, size_t workspace_bytes,
@@ -288,7 +290,16 @@ ts_status tree_attn_fwd_stall_test(const ts_attn_params* p, void* workspace, siz
   if (p && (stall_seq < 0 || stall_seq >= p->B || stall_tile < 0)) return TS_ERR_SHAPE;
   if (wait_limit_us < 100 || wait_limit_us > 1000000) return TS_ERR_UNSUPPORTED;
   return ts::attn_fwd_impl(p, workspace, workspace_bytes, stream, stall_seq, stall_tile,
-                           (unsigned long long)wait_limit_us * 1000ull);
+                           (unsigned long long)wait_limit_us * 1000ull, 0);
+}
+
+ts_status tree_attn_fwd_ctas_test(const ts_attn_params* p, void* workspace, size_t workspace_bytes, int max_ctas,
+                                  int stall_seq, int stall_tile, uint32_t wait_limit_us, ts_stream stream) {
+  if (max_ctas < 1) return TS_ERR_UNSUPPORTED;
+  if (p && (stall_seq < -1 || stall_seq >= p->B || (stall_seq >= 0 && stall_tile < 0))) return TS_ERR_SHAPE;
+  if (wait_limit_us < 100 || wait_limit_us > 1000000) return TS_ERR_UNSUPPORTED;
+  return ts::attn_fwd_impl(p, workspace, workspace_bytes, stream, stall_seq, stall_seq >= 0 ? stall_tile : 0,
+                           (unsigned long long)wait_limit_us * 1000ull, max_ctas);
 }
 
 size_t tree_verify_workspace_size(int B, int N, int V) {

@@ -7,28 +7,47 @@
 //
 // How.  For a unit (sequence b, KV head g) the G query heads of all N nodes
 // share every key, so they are packed as the M rows of the MMA:
-// row r = node * G + head_in_group.  One CTA owns one tile of 128 rows and one
-// split of the unit's prefix (a run of 128-token KV tiles); the last split
+// row r = node * G + head_in_group.  A work item is one tile of 128 rows and
+// one split of the unit's prefix (a run of 128-token KV tiles); the last split
 // also runs the tree block: the N tree keys, gated per row by the ancestry
 // bitmask.  All of these share one online softmax.
 //
-//   warp 0     TMEM allocation; TMA loads of the Q tile and of the K tiles
+// The kernel is persistent: one CTA per SM.  CTA c starts with item c; the
+// others go to whichever CTA asks first (a counter in the workspace, taken
+// by atomic add: items of unequal length, and empty splits past a short
+// prefix, then balance out by themselves).  The K producer takes the items
+// (skipping empty splits at once) and passes them to the other roles
+// through a small queue in shared memory; the rings, the S buffers and the
+// barrier phases continue from one item into the next, so the producers load
+// the next item's first tiles and the QK issuer loads its Q tile while the
+// softmax is still finishing the current one.  The counter is back at zero
+// when the kernel ends: every CTA asks until it is told there is nothing
+// left, and the last of all those requests resets it.  With one CTA per item
+// instead, the set-up before the first tile (~3 us) and the epilogue
+// (~2.5 us) were measured at 10 % of a 65-tile item and nearly 40 % of a
+// 10-tile item.
+//
+//   warp 0     TMEM allocation; TMA loads of the K tiles
 //   warp 3     TMA loads of the V tiles (paged blocks: one box per block); K
 //              and V each stream through their own ring.  At CTA start it
-//              also prefetches the tensor maps, the Q tile and the first
+//              also prefetches the tensor maps, the first Q tile and the first
 //              block-table entry into L2, ahead of the launch wait.
-//   warp 1     QK issuer (one thread): S(j) = Q K(j)^T, both operands in
-//              swizzled shared memory, into S buffer j%3 once PV(j-3) (the
-//              last reader of that buffer) has completed (s_free[j%3]).
+//   warp 1     QK issuer (one thread): loads each item's Q tile once the
+//              previous item's QKs have completed (q_empty), then
+//              S(j) = Q K(j)^T, both operands in swizzled shared memory, into
+//              S buffer j%3 once PV(j-3) (the last reader of that buffer) has
+//              completed (s_free[j%3]).
 //   warp 2     PV issuer (one thread): O += P(j) V(j), P read from TMEM, V
 //              from shared memory, as soon as the softmax has written P(j).
 //   warps 4-7  softmax: thread t owns TMEM lane t = row t.  Loads S from TMEM,
 //              masks, tracks the running max/sum, writes P (bf16) back over S,
 //              rescales O when the max moves by more than 2^20 (exact: the final
-//              normalisation uses the same running max).  At the end each
-//              thread normalises its row of O to bf16 in the idle K ring, in
+//              normalisation uses the same running max).  At the end of an
+//              item each thread normalises its row of O to bf16 and stores it:
+//              the output itself, or this split's partial.  After the CTA's
+//              last item the K ring is idle, so the rows go there instead, in
 //              the 128-byte-swizzled layout of a TMA box, and one thread
-//              stores the boxes: the output itself, or this split's partial.
+//              stores the boxes.
 //   With QK and PV on two issuers the next tile's QK^T and this tile's PV
 //   run while the softmax works.  Each control warp shares its sub-partition
 //   with a softmax warp, and the scheduler keeps issuing from a ready compute
@@ -50,7 +69,8 @@
 // role winds down.  Before the CTA frees its TMEM and exits, an aborted CTA
 // drains what it still has in flight: the producers wait (bounded) for the
 // loads they issued to land, and each MMA issuer commits to a barrier of its
-// own and waits for its MMAs to finish.  It then reports TS_ERR_TIMEOUT.
+// own and waits for its MMAs to finish.  It then reports TS_ERR_TIMEOUT for
+// the sequence of every item it had not finished.
 #include "fastexp.cuh"
 #include "internal.cuh"
 #include "sm100.cuh"
@@ -74,6 +94,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_O = 0;
 constexpr uint32_t TMEM_S0 = 128;
 constexpr int NSB = 3;  // S buffers in TMEM
+constexpr int ITEM_Q = 16;  // entries of the item queue (a role can lag the K producer by at most ~7 items)
 // O is rescaled only when a row's max rises by more than 2^20 (log2 units).
 // Until then p = 2^(s - m_run) <= 2^20: bf16 P (range to 3e38) and the fp32 O
 // and l accumulators (relative precision independent of scale) stay exact up
@@ -102,6 +123,7 @@ struct __align__(1024) Smem {
   uint8_t k[C::NSTK][C::TILE_BYTES];
   uint8_t v[C::NSTV][C::TILE_BYTES];
   uint64_t q_full;
+  uint64_t q_empty;  // the Q tile is no longer read: every QK of its item completed
   uint64_t k_full[C::NSTK];
   uint64_t v_full[C::NSTV];
   uint64_t k_empty[C::NSTK];  // K slot free: its QK completed
@@ -114,13 +136,71 @@ struct __align__(1024) Smem {
   uint32_t tmem_base;
   int abort_flag;
   int pv_done;  // PVs completed so far, published by the PV issuer (release/acquire)
+  // The CTA's items, in the order it takes them: entry k (k % ITEM_Q) holds
+  // (item, prefix length) of its k-th item, or item -1 after the last.
+  // Written by the K producer, which takes the items; items_pub entries are
+  // published, items_done items finished (stored) by the softmax.
+  int2 item_q[ITEM_Q];
+  int items_pub;
+  int items_done;
 };
 
 struct TcArgs {
   AttnArgs a;
   int box_rows;   // rows per paged TMA box: gcd(block_size, 128), so a box never crosses a block
   int direct;     // 1: a single split per unit -> write bf16 out (+ lse) directly
+  int n_items;    // row_tiles * max_splits * B * Hkv work items
+  int nodes_per_tile;  // ROW_TILE / G
+  // the launch's divisors, for divisions on the device's critical paths
+  FastDiv fd_rt, fd_ms, fd_hkv, fd_chunk, fd_bs, fd_g;
 };
+
+// A work item: row tile rt of unit (b, g), split `split`.  Items are numbered
+// unit-major, then split, then row tile: CTAs that take items one after the
+// other take the row tiles of a unit side by side (they read the same K/V
+// tiles at about the same time, from L2), and the splits of long prefixes are
+// spread over the whole order instead of gathering at its end (numbered
+// split-major, the last splits of the longest prefixes were taken last and
+// ran on alone: 103 against 93 us on 16 paged prefixes of 1-16K tokens).
+struct ItemPos {
+  int rt, split, b, g;
+};
+__device__ __forceinline__ ItemPos item_pos(int it, const TcArgs& t) {
+  ItemPos p;
+  const int rs = t.fd_rt.div(it);
+  p.rt = it - rs * t.a.row_tiles;
+  const int unit = t.fd_ms.div(rs);
+  p.split = rs - unit * t.a.max_splits;
+  p.b = t.fd_hkv.div(unit);
+  p.g = unit - p.b * t.a.Hkv;
+  return p;
+}
+
+// Its extent, once the sequence's prefix length is known.
+struct Item {
+  ItemPos pos;
+  int P;         // usable prefix length
+  int t_begin;   // first prefix tile of the split
+  int n_prefix;  // prefix tiles of this split
+  int n_tiles;   // + tree tiles on the sequence's last split
+  bool work;     // false: the split lies past this sequence's prefix
+  bool p_ok;     // false: the device prefix length had to be clamped
+};
+__device__ __forceinline__ Item make_item(int it, int p_dev, const TcArgs& t) {
+  const AttnArgs& a = t.a;
+  Item I;
+  I.pos = item_pos(it, t);
+  I.p_ok = usable_prefix(p_dev, a.chunk_tiles, a.max_splits, a.tree_split, a.bs, a.max_blocks, &I.P);
+  const int tiles = prefix_tiles(I.P);
+  // num_splits(I.P, chunk_tiles, tree_split), without its division
+  const int ps = t.fd_chunk.div(tiles + a.chunk_tiles - 1);
+  const int ns = a.tree_split ? ps + 1 : (ps == 0 ? 1 : ps);
+  I.t_begin = I.pos.split * a.chunk_tiles;
+  I.work = I.pos.split < ns;
+  I.n_prefix = max(0, min(tiles, I.t_begin + a.chunk_tiles) - I.t_begin);
+  I.n_tiles = I.n_prefix + ((I.pos.split == ns - 1) ? ceil_div(a.N, KV_TILE) : 0);
+  return I;
+}
 
 // Abort state of a CTA: its flag and the wait limit.
 struct Ctl {
@@ -188,40 +268,54 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   volatile int* abort_flag = &sm.abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rt = blockIdx.x, split = blockIdx.y, unit = blockIdx.z;
-  const int b = unit / a.Hkv, g = unit - b * a.Hkv;
-  const int t_begin = split * a.chunk_tiles;
   const Ctl ctl{abort_flag, a.wait_limit_ns};
+  const int n_items = args.n_items;
+  const int stride = gridDim.x;
+  const int first = blockIdx.x;  // < n_items: the grid has at most one CTA per item
   // Geometry of this warp's paged loads (producer warps): rows per box,
   // boxes per tile, tiles per group of 32 block-table entries.
   const int g_box = args.box_rows;
   const int g_boxes = KV_TILE / g_box;  // 1 .. 8
   const int g_tpg = 32 / g_boxes;
-  const int* table_row = a.block_table + (size_t)b * a.max_blocks;
   // First of all, by a warp that has no part in the set-up: fetch the tensor
-  // maps (kernel parameters) and prefetch into L2 the Q tile and the
-  // block-table entry of this split's first tile, so that their address
+  // maps (kernel parameters) and prefetch into L2 the first item's Q tile and
+  // the block-table entry of its first tile, so that their address
   // translation and DRAM latency overlap the set-up and the wait (prefetches
   // read no data; see sm100.cuh).
+  const ItemPos pos0 = item_pos(first, args);
   if (warp == V_PRODUCER_WARP && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kc);
     tma_prefetch_desc(&tm_vc);
     tma_prefetch_desc(&tm_kt);
     tma_prefetch_desc(&tm_vt);
-    for (int hh = 0; hh < C::HALVES; ++hh) tma_prefetch_4d(&tm_q, 64 * hh, g * a.G, rt * (ROW_TILE / a.G), b);
+    for (int hh = 0; hh < C::HALVES; ++hh) tma_prefetch_4d(&tm_q, 64 * hh, pos0.g * a.G, pos0.rt * args.nodes_per_tile, pos0.b);
     if (a.max_blocks > 0) {
       // the 16-byte piece holding the entry, through the bulk-copy unit
-      const long long idx = (long long)t_begin * KV_TILE / a.bs;
-      const uintptr_t e = reinterpret_cast<uintptr_t>(table_row + (idx < a.max_blocks ? idx : a.max_blocks - 1));
+      const int idx = args.fd_bs.div(pos0.split * a.chunk_tiles * KV_TILE);
+      const int* row0 = a.block_table + (size_t)pos0.b * a.max_blocks;
+      const uintptr_t e = reinterpret_cast<uintptr_t>(row0 + (idx < a.max_blocks ? idx : a.max_blocks - 1));
       bulk_prefetch_l2(reinterpret_cast<const void*>(e & ~uintptr_t(15)), 16);
     }
+  }
+  // the first item's first block-table entries, one per lane of a producer
+  // warp (index clamped to the table's row; entries past the prefix are
+  // discarded when used)
+  const bool producer = (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && a.max_blocks > 0;
+  const int* blk_first_addr = a.block_table;
+  if (producer) {
+    const int t0 = (pos0.split * a.chunk_tiles + lane / g_boxes) * KV_TILE + (lane % g_boxes) * g_box;
+    const int idx = args.fd_bs.div(t0);
+    blk_first_addr = a.block_table + (size_t)pos0.b * a.max_blocks + (idx < a.max_blocks ? idx : a.max_blocks - 1);
   }
 
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
     sm.pv_done = 0;
+    sm.items_pub = 0;
+    sm.items_done = 0;
     mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
     for (int i = 0; i < C::NSTK; ++i) {
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], 1);
@@ -252,37 +346,43 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   // released only at this CTA's teardown (released at the start, its CTAs
   // were measured to delay this kernel's first loads by about 2 us).
   pdl_wait();
-  // The producers fetch their first group of block-table entries together
-  // with the prefix length (index clamped to the table's row; entries past
-  // the prefix are discarded below).  Volatile loads: both are issued here,
-  // ahead of the branch on the prefix length, so their latencies overlap.
-  int blk_first = 0;
-  const bool producer = (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && a.max_blocks > 0;
-  const int* blk_addr = table_row;
-  if (producer) {
-    const long long t0 = (long long)(t_begin + lane / g_boxes) * KV_TILE + (lane % g_boxes) * g_box;
-    const long long idx = t0 / a.bs;
-    blk_addr = table_row + (idx < a.max_blocks ? idx : a.max_blocks - 1);
-  }
-  const int p_dev = ld_global_early(a.prefix_len + b);
-  if (producer) blk_first = ld_global_early(blk_addr);
-  int P;
-  const bool p_ok = usable_prefix(p_dev, a.chunk_tiles, a.max_splits, a.tree_split, a.bs, a.max_blocks, &P);
-  const int tiles = prefix_tiles(P);
-  const int ns = num_splits(P, a.chunk_tiles, a.tree_split);
-  const bool has_work = split < ns;  // splits past this sequence's prefix have nothing to do
-  if (!p_ok && threadIdx.x == 0 && rt == 0 && split == 0 && a.status) a.status[b] = TS_ERR_SHAPE;
-  const int n_prefix = max(0, min(tiles, t_begin + a.chunk_tiles) - t_begin);
-  const int n_tree = (split == ns - 1) ? ceil_div(a.N, KV_TILE) : 0;
-  const int n_tiles = n_prefix + n_tree;
+  // The producers fetch the first item's prefix length and first
+  // block-table entries together (volatile loads, issued where written), so
+  // the two latencies overlap.
+  const bool grabber = warp == PRODUCER_WARP;
+  const int p_first = grabber ? ld_global_early(a.prefix_len + pos0.b) : 0;
+  const int blk_first = producer ? ld_global_early(blk_first_addr) : 0;
 
+  // Entry k of the item queue (every role but the K producer): false if the
+  // wait gave up.
+  auto queue_entry = [&](int k, int2& e) -> bool {
+    if (!wait_count(&sm.items_pub, k + 1, ctl)) return false;
+    const volatile int* q = reinterpret_cast<volatile int*>(&sm.item_q[k % ITEM_Q]);
+    e.x = q[0];
+    e.y = q[1];
+    return true;
+  };
+  // Taking an item (lane 0 of the K producer): -1 once none is left.  The
+  // request that comes last of all (every CTA makes exactly one that finds
+  // nothing) puts the counter back to zero for the next call.
+  auto take_item = [&]() -> int {
+    const unsigned v = atomicAdd(a.sched, 1u);
+    if (v == (unsigned)(n_items - 1)) atomicExch(a.sched, 0u);
+    return stride + (int)v < n_items ? stride + (int)v : -1;
+  };
+  // K producer state the teardown of an aborted CTA needs: the item it took
+  // but has not published yet (-1: none), and whether the counter said
+  // nothing was left.
+  int held = -1;
+  bool exhausted = false;
 
   // ------------------------------------------------------------ K or V producer
   // One warp streams the K tiles, another the V tiles: a single warp issues a
   // TMA request only every ~120 cycles, so one warp alone could not keep up
   // with 16 paged boxes per tile.  Each ring slot is refilled as soon as its
-  // own consumer (QK for K, PV for V) has released it.  Returns how many
-  // tiles it issued (all of them unless a wait gave up or a stall was asked for).
+  // own consumer (QK for K, PV for V) has released it, whichever item the
+  // tile belongs to.  Returns how many tiles it issued (all of them unless a
+  // wait gave up or a stall was asked for).
   auto kv_producer = [&](bool is_v) -> int {
     const CUtensorMap* tm_pool = is_v ? &tm_vc : &tm_kc;
     const CUtensorMap* tm_node = is_v ? &tm_vt : &tm_kt;
@@ -299,320 +399,422 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     // not when it is loaded.
     const int lg_boxes = __ffs(g_boxes) - 1;
     const int koff = (lane & (g_boxes - 1)) * g_box;  // this lane's box: keys [koff, +box) of a tile
-    // Block-table entries are software-pipelined: lane L holds the entry of
-    // box (L % boxes) of tile (L / boxes) of a group of 32/boxes tiles; the
-    // next group is loaded (one coalesced read) when the current one starts,
-    // so the table's load latency hides behind several tiles of TMA issue.
-    auto load_group = [&](int grp) -> int {
-      const int tile = grp * g_tpg + (lane >> lg_boxes);
-      const int t0 = (t_begin + tile) * KV_TILE + koff;
-      if (tile >= n_prefix || t0 >= P) return 0;
-      return grp == 0 ? blk_first : table_row[t0 / a.bs];
-    };
-    int grp_cur = load_group(0);
-    int grp_nxt = (n_prefix > g_tpg) ? load_group(1) : 0;
-    const int stop = (!is_v && b == a.stall_seq) ? a.stall_tile : n_tiles;
-    // key of this lane's box in the current tile, and its row in its block
-    // (advanced by a tile, 128 mod block_size rows, each step; constant when
-    // blocks divide a tile)
-    int key = t_begin * KV_TILE + koff;
-    int row = key % a.bs;
-    const int row_step = KV_TILE % a.bs;
-    int slot = 0, phase = 0, jt = 0;  // ring slot and its phase; tile within the table group
-    int j = 0;
-    for (; j < n_tiles; ++j) {
-      uint8_t* dst = is_v ? sm.v[slot] : sm.k[slot];
-      if (j >= nst) {
+    int slot = 0, phase = 0;  // ring slot and its phase
+    int jg = 0;               // tiles issued, over every item
+    // K producer: the item in hand and its prefix length
+    int cand = first, cand_p = p_first;
+    held = first;
+    for (int k = 0;; ++k) {
+      int it, p_dev;
+      if (!is_v) {
+        // skip empty splits (a short prefix), taking the next item each time
+        for (;;) {
+          if (cand < 0 || make_item(cand, cand_p, args).work) break;
+          int nx = -1;
+          if (lane == 0) nx = take_item();
+          cand = __shfl_sync(0xffffffffu, nx, 0);
+          held = cand;
+          exhausted = cand < 0;
+          cand_p = cand >= 0 ? ld_global_early(a.prefix_len + item_pos(cand, args).b) : 0;
+        }
+        // entry k reuses entry k - ITEM_Q's slot: that item must be finished
+        bool ok = k < ITEM_Q;
+        if (!ok && lane == 0) ok = wait_count(&sm.items_done, k - ITEM_Q + 1, ctl);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return jg;
+        if (lane == 0) {
+          sm.item_q[k % ITEM_Q] = make_int2(cand, cand_p);
+          asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.items_pub)), "r"(k + 1) : "memory");
+        }
+        held = -1;
+        if (cand < 0) return jg;
+        it = cand;
+        p_dev = cand_p;
+        // take the next item now: its prefix length loads while this one streams
+        int nx = -1;
+        if (lane == 0) nx = take_item();
+        cand = __shfl_sync(0xffffffffu, nx, 0);
+        held = cand;
+        exhausted = cand < 0;
+        cand_p = cand >= 0 ? ld_global_early(a.prefix_len + item_pos(cand, args).b) : 0;
+      } else {
+        int2 e;
         bool ok = true;
-        if (lane == 0) ok = wait_bar(&empty[slot], phase ^ 1, ctl);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (lane == 0) ok = queue_entry(k, e);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return jg;
+        it = __shfl_sync(0xffffffffu, e.x, 0);
+        p_dev = __shfl_sync(0xffffffffu, e.y, 0);
+        if (it < 0) return jg;
       }
-      if (j == stop) break;
-      if (j < n_prefix) {
-        if (jt == 0 && j > 0) {
-          grp_cur = grp_nxt;
-          const int g2 = (j >> (5 - lg_boxes)) + 1;
-          grp_nxt = (g2 * g_tpg < n_prefix) ? load_group(g2) : 0;
+      const Item I = make_item(it, p_dev, args);
+      const int b = I.pos.b, g = I.pos.g, t_begin = I.t_begin, n_prefix = I.n_prefix, P = I.P;
+      const int* table_row = a.block_table + (size_t)b * a.max_blocks;
+      // Block-table entries are software-pipelined: lane L holds the entry of
+      // box (L % boxes) of tile (L / boxes) of a group of 32/boxes tiles; the
+      // next group is loaded (one coalesced read) when the current one starts,
+      // so the table's load latency hides behind several tiles of TMA issue.
+      const bool use_first = it == first;
+      auto load_group = [&](int grp) -> int {
+        const int tile = grp * g_tpg + (lane >> lg_boxes);
+        const int t0 = (t_begin + tile) * KV_TILE + koff;
+        if (tile >= n_prefix || t0 >= P) return 0;
+        return (grp == 0 && use_first) ? blk_first : table_row[args.fd_bs.div(t0)];
+      };
+      int grp_cur = load_group(0);
+      int grp_nxt = (n_prefix > g_tpg) ? load_group(1) : 0;
+      const int stop = (!is_v && b == a.stall_seq) ? a.stall_tile : I.n_tiles;
+      // key of this lane's box in the current tile, and its row in its block
+      // (advanced by a tile, 128 mod block_size rows, each step; constant when
+      // blocks divide a tile)
+      int key = t_begin * KV_TILE + koff;
+      int row = args.fd_bs.mod(key);
+      const int row_step = args.fd_bs.mod(KV_TILE);
+      int jt = 0;  // tile within the table group
+      for (int j = 0; j < I.n_tiles; ++j, ++jg) {
+        uint8_t* dst = is_v ? sm.v[slot] : sm.k[slot];
+        if (jg >= nst) {
+          bool ok = true;
+          if (lane == 0) ok = wait_bar(&empty[slot], phase ^ 1, ctl);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) return jg;
         }
-        // lane i < boxes handles the box of tokens [key, key + box_rows)
-        int blk = __shfl_sync(0xffffffffu, grp_cur, (jt << lg_boxes) + lane);
-        const bool issue = lane < g_boxes && key < P;
-        if (issue && (blk < 0 || blk >= a.num_blocks)) {
-          if (a.status) a.status[b] = TS_ERR_BAD_BLOCK;
-          blk = 0;  // read a valid block instead; the sequence is reported as failed
+        if (j == stop) return jg;
+        if (j < n_prefix) {
+          if (jt == 0 && j > 0) {
+            grp_cur = grp_nxt;
+            const int g2 = (j >> (5 - lg_boxes)) + 1;
+            grp_nxt = (g2 * g_tpg < n_prefix) ? load_group(g2) : 0;
+          }
+          // lane i < boxes handles the box of tokens [key, key + box_rows)
+          int blk = __shfl_sync(0xffffffffu, grp_cur, (jt << lg_boxes) + lane);
+          const bool issue = lane < g_boxes && key < P;
+          if (issue && (blk < 0 || blk >= a.num_blocks)) {
+            if (a.status) a.status[b] = TS_ERR_BAD_BLOCK;
+            blk = 0;  // read a valid block instead; the sequence is reported as failed
+          }
+          const unsigned mask = __ballot_sync(0xffffffffu, issue);
+          if (lane == 0) mbar_arrive_expect_tx(&full[slot], __popc(mask) * box_bytes);
+          __syncwarp();
+          // one box = every D column of box_rows tokens of one paged block
+          if (issue) tma_load_5d(dst + lane * box_bytes, tm_pool, &full[slot], 0, 0, 0, row >> 3, blk * a.Hkv + g);
+          key += KV_TILE;
+          row += row_step;
+          if (row >= a.bs) row -= a.bs;
+          jt = (jt + 1) & (g_tpg - 1);
+        } else if (lane == 0) {
+          const int n0 = (j - n_prefix) * KV_TILE;  // first tree node of this tile; nodes >= N read as zeros
+          mbar_arrive_expect_tx(&full[slot], C::TILE_BYTES);
+          for (int h = 0; h < C::HALVES; ++h) tma_load_4d(dst + h * C::HALF_BYTES, tm_node, &full[slot], 64 * h, g, n0, b);
         }
-        const unsigned mask = __ballot_sync(0xffffffffu, issue);
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], __popc(mask) * box_bytes);
         __syncwarp();
-        // one box = every D column of box_rows tokens of one paged block
-        if (issue) tma_load_5d(dst + lane * box_bytes, tm_pool, &full[slot], 0, 0, 0, row >> 3, blk * a.Hkv + g);
-        key += KV_TILE;
-        row += row_step;
-        if (row >= a.bs) row -= a.bs;
-        jt = (jt + 1) & (g_tpg - 1);
-      } else if (lane == 0) {
-        const int n0 = (j - n_prefix) * KV_TILE;  // first tree node of this tile; nodes >= N read as zeros
-        mbar_arrive_expect_tx(&full[slot], C::TILE_BYTES);
-        for (int h = 0; h < C::HALVES; ++h) tma_load_4d(dst + h * C::HALF_BYTES, tm_node, &full[slot], 64 * h, g, n0, b);
-      }
-      __syncwarp();
-      if (++slot == nst) {
-        slot = 0;
-        phase ^= 1;
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1;
+        }
       }
     }
-    return j;
   };
-  int issued = 0;  // tiles this warp's producer issued (K or V), for the drain of an aborted CTA
+  int issued = 0;                  // tiles this warp's producer issued (K or V), for the drain of an aborted CTA
+  int q_issued = 0, q_landed = 0;  // Q loads the QK issuer started / saw land, for the same drain
 
-  if (!has_work) {
-    // nothing to do; fall through to the teardown
-  } else if (warp == PRODUCER_WARP) {
-    // ------------------------------------------------------------ Q and K producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&sm.q_full, C::Q_BYTES);
-      const int nodes_per_tile = ROW_TILE / a.G;
-      for (int h = 0; h < C::HALVES; ++h)
-        tma_load_4d(sm.q + h * (ROW_TILE * 128), &tm_q, &sm.q_full, 64 * h, g * a.G, rt * nodes_per_tile, b);
-    }
-    issued = kv_producer(false);
-  } else if (warp == V_PRODUCER_WARP) {
-    issued = kv_producer(true);
+  if (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) {
+    issued = kv_producer(warp == V_PRODUCER_WARP);  // one call site: one copy of the loop
   } else if (warp == QK_WARP) {
     if (lane == 0) {
       // ---------------------------------------------------------- QK issuer
       constexpr uint32_t ID_QK = idesc_bf16_f32(ROW_TILE, KV_TILE, 0, 0);
       const uint32_t q_addr = smem_u32(sm.q);
-      bool ok = wait_bar(&sm.q_full, 0, ctl);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int slot = j % C::NSTK;
-        // K(j) has landed; S buffer j%3 is free once PV(j-3) has completed
-        // (a per-buffer barrier: it can never run two completions ahead)
-        ok = wait_bar(&sm.k_full[slot], (j / C::NSTK) & 1, ctl) &&
-             (j < NSB || wait_bar(&sm.s_free[j % NSB], ((j / NSB) - 1) & 1, ctl));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sm.k[slot]);
-        const uint32_t d_tmem = tmem + TMEM_S0 + (j % NSB) * 128;
-        // prefix tiles: D halves 1 KB apart, 8-row groups HALVES KB apart;
-        // tree tiles: D halves 16 KB apart, 8-row groups 1 KB apart
-        const bool tree = j >= n_prefix;
-        const uint32_t k_half = tree ? C::HALF_BYTES : 1024;
-        const uint32_t k_sbo = tree ? 1024 : C::HALVES * 1024;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * (ROW_TILE * 128) + (k & 3) * 32;
-          const uint32_t koff = (k >> 2) * k_half + (k & 3) * 32;
-          mma_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + koff, 16, k_sbo), ID_QK,
-                 k > 0);
+      const int nodes_per_tile = args.nodes_per_tile;
+      int jg = 0;  // tiles, over every item
+      bool ok = true;
+      auto load_q = [&](const ItemPos& q) {
+        mbar_arrive_expect_tx(&sm.q_full, C::Q_BYTES);
+        for (int h = 0; h < C::HALVES; ++h)
+          tma_load_4d(sm.q + h * (ROW_TILE * 128), &tm_q, &sm.q_full, 64 * h, q.g * a.G, q.rt * nodes_per_tile, q.b);
+        ++q_issued;
+      };
+      // The CTA's first item is `first` unless that split is empty: its Q
+      // tile needs no prefix length, so it is loaded at once.
+      load_q(pos0);
+      for (int k = 0; ok; ++k) {
+        int2 e;
+        if (!(ok = queue_entry(k, e))) break;
+        if (e.x < 0) break;
+        const Item I = make_item(e.x, e.y, args);
+        if (k > 0 || e.x != first) {
+          if (k == 0) {
+            // the tile loaded at once is not needed: let it land, free the buffer
+            if (!(ok = wait_bar(&sm.q_full, 0, ctl))) break;
+            ++q_landed;
+            mma_commit(&sm.q_empty);
+          }
+          // this item's Q tile, once every QK of the previous one has completed
+          if (!(ok = wait_bar(&sm.q_empty, (q_issued - 1) & 1, ctl))) break;
+          load_q(I.pos);
         }
-        mma_commit(&sm.s_full[j % NSB]);
-        mma_commit(&sm.k_empty[slot]);  // K(j) no longer read
+        if (!(ok = wait_bar(&sm.q_full, (q_issued - 1) & 1, ctl))) break;
+        ++q_landed;
+        for (int j = 0; j < I.n_tiles; ++j, ++jg) {
+          const int slot = jg % C::NSTK;
+          // K(j) has landed; S buffer jg%3 is free once the PV three tiles
+          // back has completed (a per-buffer barrier: it can never run two
+          // completions ahead)
+          ok = wait_bar(&sm.k_full[slot], (jg / C::NSTK) & 1, ctl) &&
+               (jg < NSB || wait_bar(&sm.s_free[jg % NSB], ((jg / NSB) - 1) & 1, ctl));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sm.k[slot]);
+          const uint32_t d_tmem = tmem + TMEM_S0 + (jg % NSB) * 128;
+          // prefix tiles: D halves 1 KB apart, 8-row groups HALVES KB apart;
+          // tree tiles: D halves 16 KB apart, 8-row groups 1 KB apart
+          const bool tree = j >= I.n_prefix;
+          const uint32_t k_half = tree ? C::HALF_BYTES : 1024;
+          const uint32_t k_sbo = tree ? 1024 : C::HALVES * 1024;
+#pragma unroll
+          for (int k2 = 0; k2 < D / 16; ++k2) {
+            const uint32_t off = (k2 >> 2) * (ROW_TILE * 128) + (k2 & 3) * 32;
+            const uint32_t koff = (k2 >> 2) * k_half + (k2 & 3) * 32;
+            mma_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + koff, 16, k_sbo), ID_QK,
+                   k2 > 0);
+          }
+          mma_commit(&sm.s_full[jg % NSB]);
+          mma_commit(&sm.k_empty[slot]);  // K(j) no longer read
+        }
+        if (ok) mma_commit(&sm.q_empty);  // Q no longer read once these QKs complete
       }
     }
   } else if (warp == PV_WARP) {
     if (lane == 0) {
       // ---------------------------------------------------------- PV issuer
       constexpr uint32_t ID_PV = idesc_bf16_f32(ROW_TILE, D, 0, 1);
-      for (int j = 0; j < n_tiles; ++j) {
-        const int slot = j % C::NSTV;
-        if (!wait_bar(&sm.p_full[j % NSB], (j / NSB) & 1, ctl)) break;
-        if (!wait_bar(&sm.v_full[slot], (j / C::NSTV) & 1, ctl)) break;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(sm.v[slot]);
-        const uint32_t p_tmem = tmem + TMEM_S0 + (j % NSB) * 128;
-        const bool tree = j >= n_prefix;
-        const uint32_t v_lbo = tree ? C::HALF_BYTES : 1024;    // between D halves
-        const uint32_t v_sbo = tree ? 1024 : C::HALVES * 1024;  // between 8-key groups
+      int jg = 0;  // tiles, over every item
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        int2 e;
+        if (!(ok = queue_entry(k, e))) break;
+        if (e.x < 0) break;
+        const Item I = make_item(e.x, e.y, args);
+        for (int j = 0; j < I.n_tiles; ++j, ++jg) {
+          const int slot = jg % C::NSTV;
+          if (!(ok = wait_bar(&sm.p_full[jg % NSB], (jg / NSB) & 1, ctl))) break;
+          if (!(ok = wait_bar(&sm.v_full[slot], (jg / C::NSTV) & 1, ctl))) break;
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(sm.v[slot]);
+          const uint32_t p_tmem = tmem + TMEM_S0 + (jg % NSB) * 128;
+          const bool tree = j >= I.n_prefix;
+          const uint32_t v_lbo = tree ? C::HALF_BYTES : 1024;    // between D halves
+          const uint32_t v_sbo = tree ? 1024 : C::HALVES * 1024;  // between 8-key groups
 #pragma unroll
-        for (int k = 0; k < KV_TILE / 16; ++k)
-          mma_ts(tmem + TMEM_O, p_tmem + k * 8, smem_desc_sw128(v_addr + k * 2 * v_sbo, v_lbo, v_sbo), ID_PV,
-                 j > 0 || k > 0);
-        mma_commit(&sm.o_ready);
-        mma_commit(&sm.s_free[j % NSB]);
-        mma_commit(&sm.v_empty[slot]);  // V(j) no longer read
-        // wait for PV(j) here (every phase in order) and publish the count, so
-        // the softmax looks at O only when it has to rescale it
-        if (!wait_bar(&sm.o_ready, j & 1, ctl)) break;
-        tc_fence_after();
-        asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.pv_done)), "r"(j + 1) : "memory");
+          for (int k2 = 0; k2 < KV_TILE / 16; ++k2)
+            mma_ts(tmem + TMEM_O, p_tmem + k2 * 8, smem_desc_sw128(v_addr + k2 * 2 * v_sbo, v_lbo, v_sbo), ID_PV,
+                   j > 0 || k2 > 0);
+          mma_commit(&sm.o_ready);
+          mma_commit(&sm.s_free[jg % NSB]);
+          mma_commit(&sm.v_empty[slot]);  // V(j) no longer read
+          // wait for this PV here (every phase in order) and publish the
+          // count, so the softmax looks at O only when it has to rescale it
+          // or, at the end of an item, read it
+          if (!(ok = wait_bar(&sm.o_ready, jg & 1, ctl))) break;
+          tc_fence_after();
+          asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.pv_done)), "r"(jg + 1) : "memory");
+        }
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
     const int r = threadIdx.x - SOFTMAX_WARP0 * 32;  // TMEM lane == packed row within the tile
     const int R = a.N * a.G;
-    const int grow = rt * ROW_TILE + r;
-    const bool active = grow < R;
-    const int node = active ? grow / a.G : 0;
-    const int h = g * a.G + (active ? grow - node * a.G : 0);
-    // ancestry words of this row; words past W stay zero.  Padding rows (past
-    // N*G) see every key so that their softmax stays finite; never written out.
-    uint64_t anc[4] = {0ull, 0ull, 0ull, 0ull};
-    if (active) {
-      for (int w = 0; w < a.W; ++w) anc[w] = a.anc_mask[((size_t)b * a.N + node) * a.W + w];
-    } else {
-      anc[0] = anc[1] = anc[2] = anc[3] = ~0ull;
-    }
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    float m_run = NEG_INF, l_run = 0.f;
+    const size_t rows_all = (size_t)a.B * a.N * a.Hq;
+    int jg = 0;  // tiles, over every item
     bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      if (!__all_sync(0xffffffffu, wait_bar(&sm.s_full[j % NSB], (j / NSB) & 1, ctl))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t s_tmem = tmem + lane_base + TMEM_S0 + (j % NSB) * 128;
-      float s[KV_TILE];
-      {
-        // all four TMEM loads in flight before one wait
-        uint32_t u[KV_TILE / 32][32];
-#pragma unroll
-        for (int c = 0; c < KV_TILE / 32; ++c) tmem_ld32(s_tmem + c * 32, u[c]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < KV_TILE / 32; ++c) {
-          reg_fence32(u[c]);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(u[c][e]);
-        }
-      }
-      // masking: ragged prefix tail, or the tree block's ancestry bits
-      bool tail_zero_v = false;
-      int valid = KV_TILE;
-      if (j < n_prefix) {
-        const int key0 = (t_begin + j) * KV_TILE;
-        valid = min(KV_TILE, P - key0);
-        if (valid < KV_TILE) {
-          tail_zero_v = true;
-#pragma unroll
-          for (int c = 0; c < KV_TILE; ++c)
-            if (c >= valid) s[c] = NEG_INF;
-        }
+    // the CTA's last item ends in the idle K ring, stored by TMA boxes after
+    // the loop (every softmax thread reaches that barrier, whatever happens)
+    bool staged = false;
+    ItemPos last_pos{0, 0, 0, 0};
+    uint8_t* stage = &sm.k[0][0];
+    int2 e;
+    ok = queue_entry(0, e);
+    for (int k = 0; ok && e.x >= 0; ++k) {
+      const Item I = make_item(e.x, e.y, args);
+      const int b = I.pos.b, g = I.pos.g, rt = I.pos.rt, split = I.pos.split;
+      const int t_begin = I.t_begin, n_prefix = I.n_prefix, P = I.P;
+      if (!I.p_ok && r == 0 && rt == 0 && split == 0 && a.status) a.status[b] = TS_ERR_SHAPE;
+      const int grow = rt * ROW_TILE + r;
+      const bool active = grow < R;
+      const int node = active ? args.fd_g.div(grow) : 0;
+      const int h = g * a.G + (active ? grow - node * a.G : 0);
+      // ancestry words of this row; words past W stay zero.  Padding rows (past
+      // N*G) see every key so that their softmax stays finite; never written out.
+      uint64_t anc[4] = {0ull, 0ull, 0ull, 0ull};
+      if (active) {
+        for (int w = 0; w < a.W; ++w) anc[w] = a.anc_mask[((size_t)b * a.N + node) * a.W + w];
       } else {
-        const int tt = j - n_prefix;  // tree tile: nodes [128*tt, 128*tt + 128)
-        const uint64_t lo = tt == 0 ? anc[0] : (tt == 1 ? anc[2] : 0ull);
-        const uint64_t hi = tt == 0 ? anc[1] : (tt == 1 ? anc[3] : 0ull);
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (!((lo >> c) & 1ull)) s[c] = NEG_INF;
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (!((hi >> c) & 1ull)) s[64 + c] = NEG_INF;
+        anc[0] = anc[1] = anc[2] = anc[3] = ~0ull;
       }
-      // row max with 8 independent chains, then a 3-level tree
-      float mk[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mk[e] = s[e];
-#pragma unroll
-      for (int c = 8; c < KV_TILE; c += 8)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mk[e] = fmaxf(mk[e], s[c + e]);
-      float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
-      mx *= a.scale_log2;
-      const float m_new = fmaxf(m_run, mx);
-      const bool rescale = (j > 0) && (m_new > m_run + RESCALE_THRESHOLD);
-      float m_use = m_run;
-      if (j == 0 || rescale) m_use = m_new;
-      // nothing visible so far: every p is 0 (and O is rescaled away later)
-      const float m_exp = (m_use == NEG_INF) ? 0.f : m_use;
-      // p = 2^(s*scale*log2e - m), packed to bf16 pairs and written over S
-      // x = s * scale * log2(e) - m and the running sums on packed pairs
-      // (one f32x2 instruction per two scores), p = 2^x on the ex2 unit
-      const uint64_t scale2 = fx::pack2(a.scale_log2, a.scale_log2);
-      const uint64_t negm2 = fx::pack2(-m_exp, -m_exp);
-      uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // 4 independent packed partial sums
-      uint32_t pk[KV_TILE / 2];
-#pragma unroll
-      for (int e = 0; e < KV_TILE / 2; ++e) {
-        float x0, x1;
-        fx::unpack2(fx::fma2(fx::pack2(s[2 * e], s[2 * e + 1]), scale2, negm2), x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        sum2[e & 3] = fx::add2(sum2[e & 3], fx::pack2(p0, p1));
-        pk[e] = pack_bf16x2(p0, p1);
-      }
-      float rowsum;
-      {
-        float r0, r1;
-        fx::unpack2(fx::add2(fx::add2(sum2[0], sum2[1]), fx::add2(sum2[2], sum2[3])), r0, r1);
-        rowsum = r0 + r1;
-      }
-      {
-        uint32_t part[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) part[e] = pk[e];
-        tmem_st32(s_tmem, part);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) part[e] = pk[32 + e];
-        tmem_st32(s_tmem + 32, part);
-      }
-      if (tail_zero_v) {
-        // rows >= valid of this V tile hold whatever the pool had past the
-        // prefix (or stale data): zero them so 0 * V can never be NaN
-        const int slot = j % C::NSTV;
-        if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[slot], (j / C::NSTV) & 1, ctl))) {
-          ok = false;
-          break;
-        }
-        if (r >= valid) {
-          for (int hh = 0; hh < C::HALVES; ++hh) {
-            uint4* row = reinterpret_cast<uint4*>(sm.v[slot] + ((r >> 3) * C::HALVES + hh) * 1024 + (r & 7) * 128);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O must hold PV(0..j-1) complete before it is rescaled.  TMEM loads
-        // and stores are warp-collective: the whole warp rescales its rows
-        // together, with factor 1 for rows whose max did not move enough.
-        if (!__all_sync(0xffffffffu, wait_count(&sm.pv_done, j, ctl))) {
+      float m_run = NEG_INF, l_run = 0.f;
+      for (int j = 0; j < I.n_tiles; ++j, ++jg) {
+        if (!__all_sync(0xffffffffu, wait_bar(&sm.s_full[jg % NSB], (jg / NSB) & 1, ctl))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t s_tmem = tmem + lane_base + TMEM_S0 + (jg % NSB) * 128;
+        float s[KV_TILE];
         {
-          const float f = !rescale ? 1.f : ((m_run == NEG_INF) ? 0.f : ex2(m_run - m_new));
-          l_run *= f;
+          // all four TMEM loads in flight before one wait
+          uint32_t u[KV_TILE / 32][32];
 #pragma unroll
-          for (int c = 0; c < D; c += 64) {
-            uint32_t u0[32], u1[32];
-            tmem_ld32(tmem + lane_base + TMEM_O + c, u0);
-            if (c + 32 < D) tmem_ld32(tmem + lane_base + TMEM_O + c + 32, u1);
-            tmem_ld_wait();
-            reg_fence32(u0);
-            reg_fence32(u1);
+          for (int c = 0; c < KV_TILE / 32; ++c) tmem_ld32(s_tmem + c * 32, u[c]);
+          tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) u0[e] = __float_as_uint(__uint_as_float(u0[e]) * f);
+          for (int c = 0; c < KV_TILE / 32; ++c) {
+            reg_fence32(u[c]);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) u1[e] = __float_as_uint(__uint_as_float(u1[e]) * f);
-            tmem_st32(tmem + lane_base + TMEM_O + c, u0);
-            if (c + 32 < D) tmem_st32(tmem + lane_base + TMEM_O + c + 32, u1);
+            for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(u[c][e]);
           }
         }
+        // masking: ragged prefix tail, or the tree block's ancestry bits
+        bool tail_zero_v = false;
+        int valid = KV_TILE;
+        if (j < n_prefix) {
+          const int key0 = (t_begin + j) * KV_TILE;
+          valid = min(KV_TILE, P - key0);
+          if (valid < KV_TILE) {
+            tail_zero_v = true;
+#pragma unroll
+            for (int c = 0; c < KV_TILE; ++c)
+              if (c >= valid) s[c] = NEG_INF;
+          }
+        } else {
+          const int tt = j - n_prefix;  // tree tile: nodes [128*tt, 128*tt + 128)
+          const uint64_t lo = tt == 0 ? anc[0] : (tt == 1 ? anc[2] : 0ull);
+          const uint64_t hi = tt == 0 ? anc[1] : (tt == 1 ? anc[3] : 0ull);
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (!((lo >> c) & 1ull)) s[c] = NEG_INF;
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (!((hi >> c) & 1ull)) s[64 + c] = NEG_INF;
+        }
+        // row max with 8 independent chains, then a 3-level tree
+        float mk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mk[e] = s[e];
+#pragma unroll
+        for (int c = 8; c < KV_TILE; c += 8)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mk[e] = fmaxf(mk[e], s[c + e]);
+        float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+        mx *= a.scale_log2;
+        const float m_new = fmaxf(m_run, mx);
+        const bool rescale = (j > 0) && (m_new > m_run + RESCALE_THRESHOLD);
+        float m_use = m_run;
+        if (j == 0 || rescale) m_use = m_new;
+        // nothing visible so far: every p is 0 (and O is rescaled away later)
+        const float m_exp = (m_use == NEG_INF) ? 0.f : m_use;
+        // p = 2^(s*scale*log2e - m), packed to bf16 pairs and written over S
+        // x = s * scale * log2(e) - m and the running sums on packed pairs
+        // (one f32x2 instruction per two scores), p = 2^x on the ex2 unit
+        const uint64_t scale2 = fx::pack2(a.scale_log2, a.scale_log2);
+        const uint64_t negm2 = fx::pack2(-m_exp, -m_exp);
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // 4 independent packed partial sums
+        uint32_t pk[KV_TILE / 2];
+#pragma unroll
+        for (int e = 0; e < KV_TILE / 2; ++e) {
+          float x0, x1;
+          fx::unpack2(fx::fma2(fx::pack2(s[2 * e], s[2 * e + 1]), scale2, negm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum2[e & 3] = fx::add2(sum2[e & 3], fx::pack2(p0, p1));
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        float rowsum;
+        {
+          float r0, r1;
+          fx::unpack2(fx::add2(fx::add2(sum2[0], sum2[1]), fx::add2(sum2[2], sum2[3])), r0, r1);
+          rowsum = r0 + r1;
+        }
+        {
+          uint32_t part[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) part[e] = pk[e];
+          tmem_st32(s_tmem, part);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) part[e] = pk[32 + e];
+          tmem_st32(s_tmem + 32, part);
+        }
+        if (tail_zero_v) {
+          // rows >= valid of this V tile hold whatever the pool had past the
+          // prefix (or stale data): zero them so 0 * V can never be NaN
+          const int slot = jg % C::NSTV;
+          if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[slot], (jg / C::NSTV) & 1, ctl))) {
+            ok = false;
+            break;
+          }
+          if (r >= valid) {
+            for (int hh = 0; hh < C::HALVES; ++hh) {
+              uint4* row = reinterpret_cast<uint4*>(sm.v[slot] + ((r >> 3) * C::HALVES + hh) * 1024 + (r & 7) * 128);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+          // O must hold every earlier PV complete before it is rescaled.  TMEM loads
+          // and stores are warp-collective: the whole warp rescales its rows
+          // together, with factor 1 for rows whose max did not move enough.
+          if (!__all_sync(0xffffffffu, wait_count(&sm.pv_done, jg, ctl))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          {
+            const float f = !rescale ? 1.f : ((m_run == NEG_INF) ? 0.f : ex2(m_run - m_new));
+            l_run *= f;
+#pragma unroll
+            for (int c = 0; c < D; c += 64) {
+              uint32_t u0[32], u1[32];
+              tmem_ld32(tmem + lane_base + TMEM_O + c, u0);
+              if (c + 32 < D) tmem_ld32(tmem + lane_base + TMEM_O + c + 32, u1);
+              tmem_ld_wait();
+              reg_fence32(u0);
+              reg_fence32(u1);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) u0[e] = __float_as_uint(__uint_as_float(u0[e]) * f);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) u1[e] = __float_as_uint(__uint_as_float(u1[e]) * f);
+              tmem_st32(tmem + lane_base + TMEM_O + c, u0);
+              if (c + 32 < D) tmem_st32(tmem + lane_base + TMEM_O + c + 32, u1);
+            }
+          }
+        }
+        m_run = m_use;
+        l_run += rowsum;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[jg % NSB]);
       }
-      m_run = m_use;
-      l_run += rowsum;
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.p_full[j % NSB]);
-    }
-    // epilogue: wait for the last PV, normalise, stage the rows in shared
-    // memory as TMA boxes (128-byte rows, 16-byte chunk k of row r at
-    // k ^ (r % 8): the 128-byte swizzle, and conflict-free for these writes),
-    // then one thread stores the boxes.  The K ring is idle by now: every QK
-    // has completed before the last PV could start.
-    const bool epi = ok && __all_sync(0xffffffffu, wait_count(&sm.pv_done, n_tiles, ctl));
-    uint8_t* stage = &sm.k[0][0];
-    float lse2 = 0.f;
-    if (epi) {
+      if (!ok) break;
+      // end of the item: wait for its last PV, normalise, store; and see
+      // whether another item follows
+      int2 e_next;
+      const bool epi = __all_sync(0xffffffffu, wait_count(&sm.pv_done, jg, ctl) && queue_entry(k + 1, e_next));
+      if (!epi) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const float inv = 1.f / l_run;
-      lse2 = m_run + __log2f(l_run);
-      // bf16 boxes of 64 columns (one per D half), each 128 rows of 128
-      // bytes; columns c .. c+31 are chunks (c % 64) / 8 .. +3 of box c / 64.
+      const float lse2 = m_run + __log2f(l_run);
+      const size_t orow = ((size_t)b * a.N + node) * a.Hq + h;
+      // The CTA's last item goes to the idle K ring (every QK has completed
+      // before the last PV could start) as bf16 TMA boxes of 64 columns (one
+      // per D half), each 128 rows of 128 bytes: columns c .. c+31 are
+      // chunks (c % 64) / 8 .. +3 of box c / 64, chunk k of row r at
+      // k ^ (r % 8) (the 128-byte swizzle, conflict-free for these writes).
+      // Any other item writes its rows straight to global memory (the rings
+      // carry the next items' tiles), 16 bytes a store.
+      const bool to_stage = e_next.x < 0;
+      __nv_bfloat16* dst = args.direct ? a.out + orow * D : a.part_o + ((size_t)split * rows_all + orow) * D;
       // The loop is kept rolled: unrolled, it changed how the softmax loop
       // above was compiled, which then ran 10% slower on long prefixes.
 #pragma unroll 1
@@ -620,43 +822,55 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         uint32_t u[32];
         tmem_ld32(tmem + lane_base + TMEM_O + c, u);
         tmem_ld_wait();
-        uint8_t* row = stage + (c / 64) * (ROW_TILE * 128) + r * 128;
+        uint8_t* srow = stage + (c / 64) * (ROW_TILE * 128) + r * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int k = (c % 64) / 8 + q;
           uint4 v;
           v.x = pack_bf16x2(__uint_as_float(u[8 * q + 0]) * inv, __uint_as_float(u[8 * q + 1]) * inv);
           v.y = pack_bf16x2(__uint_as_float(u[8 * q + 2]) * inv, __uint_as_float(u[8 * q + 3]) * inv);
           v.z = pack_bf16x2(__uint_as_float(u[8 * q + 4]) * inv, __uint_as_float(u[8 * q + 5]) * inv);
           v.w = pack_bf16x2(__uint_as_float(u[8 * q + 6]) * inv, __uint_as_float(u[8 * q + 7]) * inv);
-          *reinterpret_cast<uint4*>(row + ((k ^ (r & 7)) << 4)) = v;
+          if (to_stage)
+            *reinterpret_cast<uint4*>(srow + ((((c % 64) / 8 + q) ^ (r & 7)) << 4)) = v;
+          else if (active)
+            reinterpret_cast<uint4*>(dst + c)[q] = v;
         }
-      }
-      fence_proxy_async();
-    }
-    // every softmax thread reaches this barrier, whatever happened above
-    const bool all_epi = named_barrier_and(1, SOFTMAX_THREADS, epi);
-    if (all_epi) {
-      if (r == 0) {
-        // rows of nodes >= N fall outside the tensor and are not written
-        const int node0 = rt * (ROW_TILE / a.G);
-        for (int hh = 0; hh < C::HALVES; ++hh) {
-          if (args.direct)
-            tma_store_4d(&tm_o, stage + hh * (ROW_TILE * 128), 64 * hh, g * a.G, node0, b);
-          else
-            tma_store_5d(&tm_po, stage + hh * (ROW_TILE * 128), 64 * hh, g * a.G, node0, b, split);
-        }
-        bulk_commit_group();
-        bulk_wait_read_all();
       }
       if (active) {
-        const size_t orow = ((size_t)b * a.N + node) * a.Hq + h;
         if (args.direct) {
           if (a.lse) a.lse[orow] = lse2 * 0.69314718055994531f;
         } else {
-          a.part_lse[(size_t)split * ((size_t)a.B * a.N * a.Hq) + orow] = lse2;
+          a.part_lse[(size_t)split * rows_all + orow] = lse2;
         }
       }
+      if (to_stage) {
+        fence_proxy_async();
+        staged = true;
+        last_pos = I.pos;
+      } else {
+        // O has been read: the next item's first PV may overwrite it (it
+        // waits for that item's first P, which follows in program order)
+        tc_fence_before();
+        __syncwarp();
+        if (r == 0) asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.items_done)), "r"(k + 1) : "memory");
+      }
+      e = e_next;
+    }
+    // every softmax thread reaches this barrier, whatever happened above
+    const bool all_staged = named_barrier_and(1, SOFTMAX_THREADS, staged);
+    if (all_staged && r == 0) {
+      // rows of nodes >= N fall outside the tensor and are not written
+      const int node0 = last_pos.rt * args.nodes_per_tile;
+      for (int hh = 0; hh < C::HALVES; ++hh) {
+        if (args.direct)
+          tma_store_4d(&tm_o, stage + hh * (ROW_TILE * 128), 64 * hh, last_pos.g * a.G, node0, last_pos.b);
+        else
+          tma_store_5d(&tm_po, stage + hh * (ROW_TILE * 128), 64 * hh, last_pos.g * a.G, node0, last_pos.b,
+                       last_pos.split);
+      }
+      bulk_commit_group();
+      bulk_wait_read_all();
+      asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.items_done)), "r"(0x7fffffff) : "memory");
     }
   }
 
@@ -666,23 +880,41 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     // A wait gave up.  Nothing may still write this CTA's shared memory or
     // TMEM once it exits: wait (bounded, regardless of the flag) for the last
     // loads each producer issued (only the newest tiles of a ring, as many
-    // as it has slots, can be outstanding) and for every MMA each issuer
-    // started.
+    // as it has slots, can be outstanding), for a Q tile still on its way,
+    // and for every MMA each issuer started.
     if ((warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && lane == 0) {
       uint64_t* full = warp == PRODUCER_WARP ? sm.k_full : sm.v_full;
       const int nst = warp == PRODUCER_WARP ? C::NSTK : C::NSTV;
-      if (warp == PRODUCER_WARP && has_work) mbar_wait(&sm.q_full, 0, a.wait_limit_ns);
       for (int j = max(0, issued - nst); j < issued; ++j) mbar_wait(&full[j % nst], (j / nst) & 1, a.wait_limit_ns);
     } else if ((warp == QK_WARP || warp == PV_WARP) && lane == 0) {
+      if (q_issued > q_landed) mbar_wait(&sm.q_full, (q_issued - 1) & 1, a.wait_limit_ns);
       uint64_t* d = &sm.drain[warp - QK_WARP];
       mma_commit(d);
       mbar_wait(d, 0, a.wait_limit_ns);
     }
     tc_fence_before();
     __syncthreads();
+    // Every item this CTA took and did not finish reports the timeout for
+    // its sequence: those published and not finished, the one the K producer
+    // holds, and (so that the counter still ends at zero) every item it
+    // takes from now on.
+    if (threadIdx.x == 0) {
+      auto report = [&](int it) {
+        if (it < 0 || !a.status) return;
+        const Item I = make_item(it, a.prefix_len[item_pos(it, args).b], args);
+        if (I.work) a.status[I.pos.b] = TS_ERR_TIMEOUT;
+      };
+      const int pub = sm.items_pub, done = sm.items_done;
+      for (int k = done; k < pub && k < done + ITEM_Q; ++k) report(sm.item_q[k % ITEM_Q].x);
+      report(held);
+      while (!exhausted) {
+        const int it = take_item();
+        exhausted = it < 0;
+        report(it);
+      }
+    }
   }
   pdl_trigger();
-  if (sm.abort_flag && threadIdx.x == 0 && a.status) a.status[b] = TS_ERR_TIMEOUT;
   if (warp == PRODUCER_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -694,6 +926,20 @@ constexpr size_t smem_bytes() {
   return sizeof(Smem<D>) + 1024;  // + alignment slack for the 1024-byte swizzle atoms
 }
 
+// Streaming multiprocessors of the current device (queried once per device).
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev < 0 || dev >= 64) return -1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 template <int D>
 cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   TcArgs t{};
@@ -701,6 +947,14 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   t.box_rows = KV_TILE;  // gcd(block_size, 128): block sizes are multiples of 16
   while (a.bs % t.box_rows != 0) t.box_rows >>= 1;
   t.direct = a.max_splits == 1;
+  t.n_items = a.row_tiles * a.max_splits * a.B * a.Hkv;
+  t.nodes_per_tile = ROW_TILE / a.G;
+  t.fd_rt = FastDiv::make(a.row_tiles);
+  t.fd_ms = FastDiv::make(a.max_splits);
+  t.fd_hkv = FastDiv::make(a.Hkv);
+  t.fd_chunk = FastDiv::make(a.chunk_tiles);
+  t.fd_bs = FastDiv::make(a.bs);
+  t.fd_g = FastDiv::make(a.G);
   CUtensorMap m_q, m_kc, m_vc, m_kt, m_vt;
   // q [B, N, Hq, D]: dims (D, Hq, N, B); box (64, G, 128/G, 1) = 128 packed rows
   {
@@ -744,7 +998,12 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
     const uint32_t box[5] = {64, (uint32_t)a.G, (uint32_t)(ROW_TILE / a.G), 1, 1};
     if (!encode_bf16_sw128(&m_po, a.part_o, 5, dims, str, box)) return cudaErrorInvalidValue;
   }
-  dim3 grid(a.row_tiles, a.max_splits, a.B * a.Hkv);
+  // persistent: one CTA per SM (each holds ~225 KB of shared memory), or one
+  // per item when there are fewer
+  int ctas = sm_count();
+  if (ctas <= 0) return cudaErrorInvalidDevice;
+  if (a.max_ctas > 0 && a.max_ctas < ctas) ctas = a.max_ctas;
+  dim3 grid(t.n_items < ctas ? t.n_items : ctas);
   return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt, m_o,
                     m_po);
 }

@@ -44,6 +44,33 @@ constexpr int PLAN_SMS = 152;  // GB300: the planner sizes grids for 152 SMs
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Division by a divisor fixed for a whole launch, for numerators in [0, 2^31),
+// by a multiply-high, an add and a shift instead of the ~30-instruction
+// integer division: with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (umulhi(n, m) + n) >> l (the round-up method of Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994;
+// n < 2^31 keeps the sum within 32 bits).
+struct FastDiv {
+  uint32_t m = 1, l = 0;
+  int d = 1;
+  static FastDiv make(int d) {
+    FastDiv f;
+    f.d = d;
+    while ((1ull << f.l) < (unsigned long long)d) ++f.l;
+    f.m = (uint32_t)((((1ull << 32) * ((1ull << f.l) - (unsigned long long)d)) / (unsigned long long)d) + 1ull);
+    return f;
+  }
+  __host__ __device__ int div(int n) const {
+#ifdef __CUDA_ARCH__
+    const uint32_t t = __umulhi((uint32_t)n, m);
+#else
+    const uint32_t t = (uint32_t)(((unsigned long long)(uint32_t)n * m) >> 32);
+#endif
+    return (int)((t + (uint32_t)n) >> l);
+  }
+  __host__ __device__ int mod(int n) const { return n - div(n) * d; }
+};
+
 // Number of prefix tiles of a sequence, and how many splits its prefix is cut
 // into when every split takes `chunk_tiles` tiles.  The tree block rides on
 // the LAST split of a sequence: with tree_split = 0 that is the last prefix
@@ -85,6 +112,7 @@ struct AttnArgs {
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
+  unsigned* sched;         // item counter of the persistent attention kernel: zero before and after a call
   __nv_bfloat16* part_o;  // [max_splits, B*N*Hq, D] bf16, normalised partial outputs
   float* part_lse;  // [max_splits, B*N*Hq] fp32, base-2 log-sum-exp of each partial
   int B, N, Hq, Hkv, G, D, W;
@@ -100,8 +128,10 @@ struct AttnArgs {
   // so the wait for that tile runs out with nothing in flight.
   unsigned long long wait_limit_ns;
   int stall_seq, stall_tile;
+  int max_ctas;  // > 0: at most this many CTAs of the persistent kernel (testing); else one per SM
 };
 constexpr unsigned long long ATTN_WAIT_LIMIT_NS = 200000000ull;  // 200 ms: far above any legitimate wait
+constexpr size_t ATTN_SCHED_BYTES = 256;  // head of the attention workspace: the item counter
 
 struct AttnPlan {
   int chunk_tiles;

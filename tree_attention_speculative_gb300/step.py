@@ -109,7 +109,8 @@ class TreeVerifyStep:
         if need == 0:
             raise ValueError("tree_attn_fwd would reject these arguments")
         if self.ws_attn is None or self.ws_attn.numel() < need:
-            self.ws_attn = torch.empty(need, dtype=torch.uint8, device=self.device)
+            # zero-filled once; every call leaves its head (the item counter) zero again
+            self.ws_attn = torch.zeros(need, dtype=torch.uint8, device=self.device)
         tree_attn_fwd(p, self.ws_attn, stream)
 
     def verify(self, draft, logits, parent, stream=None):
