@@ -151,6 +151,7 @@ struct TcArgs {
   int direct;     // 1: a single split per unit -> write bf16 out (+ lse) directly
   int n_items;    // row_tiles * max_splits * B * Hkv work items
   int nodes_per_tile;  // ROW_TILE / G
+  int out32;           // the output (or the partials) start on a 32-byte boundary
   // the launch's divisors, for divisions on the device's critical paths
   FastDiv fd_rt, fd_ms, fd_hkv, fd_chunk, fd_bs, fd_g;
 };
@@ -247,6 +248,13 @@ __device__ __forceinline__ int ld_global_early(const int* p) {
   int v;
   asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(reinterpret_cast<uint64_t>(p)) : "memory");
   return v;
+}
+
+// One 32-byte store of 8 words (a whole DRAM sector), to a 32-byte aligned address.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -552,8 +560,24 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         }
         if (!(ok = wait_bar(&sm.q_full, (q_issued - 1) & 1, ctl))) break;
         ++q_landed;
+        bool next_q_seen = false;
         for (int j = 0; j < I.n_tiles; ++j, ++jg) {
           const int slot = jg % C::NSTK;
+          if (!next_q_seen) {
+            // once the next item is known (the K producer names it after its
+            // last K tile of this one), its Q tile goes into L2
+            int pub;
+            asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(pub) : "r"(smem_u32(&sm.items_pub)) : "memory");
+            if (pub > k + 1) {
+              next_q_seen = true;
+              const int nx = sm.item_q[(k + 1) % ITEM_Q].x;
+              if (nx >= 0) {
+                const ItemPos pn = item_pos(nx, args);
+                for (int h = 0; h < C::HALVES; ++h)
+                  tma_prefetch_4d(&tm_q, 64 * h, pn.g * a.G, pn.rt * nodes_per_tile, pn.b);
+              }
+            }
+          }
           // K(j) has landed; S buffer jg%3 is free once the PV three tiles
           // back has completed (a per-buffer barrier: it can never run two
           // completions ahead)
@@ -823,17 +847,26 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         tmem_ld32(tmem + lane_base + TMEM_O + c, u);
         tmem_ld_wait();
         uint8_t* srow = stage + (c / 64) * (ROW_TILE * 128) + r * 128;
+        uint32_t w[16];  // the 32 columns as bf16 pairs
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(u[8 * q + 0]) * inv, __uint_as_float(u[8 * q + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(u[8 * q + 2]) * inv, __uint_as_float(u[8 * q + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(u[8 * q + 4]) * inv, __uint_as_float(u[8 * q + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(u[8 * q + 6]) * inv, __uint_as_float(u[8 * q + 7]) * inv);
-          if (to_stage)
-            *reinterpret_cast<uint4*>(srow + ((((c % 64) / 8 + q) ^ (r & 7)) << 4)) = v;
-          else if (active)
-            reinterpret_cast<uint4*>(dst + c)[q] = v;
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+        if (to_stage) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(srow + ((((c % 64) / 8 + q) ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        } else if (active) {
+          // a row's 64 bytes here: two 32-byte stores where the output is
+          // 32-byte aligned (each a whole DRAM sector), else four of 16
+          if (args.out32) {
+            st_global_v8(dst + c, w);
+            st_global_v8(dst + c + 16, w + 8);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              reinterpret_cast<uint4*>(dst + c)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
         }
       }
       if (active) {
@@ -949,6 +982,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   t.direct = a.max_splits == 1;
   t.n_items = a.row_tiles * a.max_splits * a.B * a.Hkv;
   t.nodes_per_tile = ROW_TILE / a.G;
+  t.out32 = (reinterpret_cast<uintptr_t>(t.direct ? (const void*)a.out : (const void*)a.part_o) & 31) == 0;
   t.fd_rt = FastDiv::make(a.row_tiles);
   t.fd_ms = FastDiv::make(a.max_splits);
   t.fd_hkv = FastDiv::make(a.Hkv);
