@@ -668,9 +668,16 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       const int h = g * a.G + (active ? grow - node * a.G : 0);
       // ancestry words of this row; words past W stay zero.  Padding rows (past
       // N*G) see every key so that their softmax stays finite; never written out.
+      // Unrolled with fixed indices, so the words stay in registers and the
+      // loads are waited for only at the tree tile: a loop over a.W put them in
+      // local memory, and with it the end of one item to the first tile of the
+      // next took 0.70 us on the 64-sequence, 8K-prefix layer (0.45 now).
       uint64_t anc[4] = {0ull, 0ull, 0ull, 0ull};
       if (active) {
-        for (int w = 0; w < a.W; ++w) anc[w] = a.anc_mask[((size_t)b * a.N + node) * a.W + w];
+        const uint64_t* arow = a.anc_mask + ((size_t)b * a.N + node) * a.W;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          if (w < a.W) anc[w] = arow[w];
       } else {
         anc[0] = anc[1] = anc[2] = anc[3] = ~0ull;
       }
