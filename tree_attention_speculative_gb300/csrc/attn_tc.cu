@@ -443,17 +443,6 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     // K producer: the item in hand and its prefix length
     int cand = first, cand_p = p_first;
     held = first;
-    // Take the next item (K producer): its prefix length then loads while
-    // this one streams.  Done after the item's first TMA loads are issued, so
-    // that the counter's round trip does not delay them.
-    auto take_next = [&]() {
-      int nx = -1;
-      if (lane == 0) nx = take_item();
-      cand = __shfl_sync(0xffffffffu, nx, 0);
-      held = cand;
-      exhausted = cand < 0;
-      cand_p = cand >= 0 ? ld_global_early(a.prefix_len + item_pos(cand, args).b) : 0;
-    };
     for (int k = 0;; ++k) {
       int it, p_dev;
       if (!is_v) {
@@ -479,7 +468,13 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         if (cand < 0) return jg;
         it = cand;
         p_dev = cand_p;
-        cand = -2;  // the next item is taken once this one's first tile is on its way
+        // take the next item now: its prefix length loads while this one streams
+        int nx = -1;
+        if (lane == 0) nx = take_item();
+        cand = __shfl_sync(0xffffffffu, nx, 0);
+        held = cand;
+        exhausted = cand < 0;
+        cand_p = cand >= 0 ? ld_global_early(a.prefix_len + item_pos(cand, args).b) : 0;
       } else {
         int2 e;
         bool ok = true;
@@ -553,9 +548,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
           slot = 0;
           phase ^= 1;
         }
-        if (!is_v && j == 0) take_next();
       }
-      if (!is_v && cand == -2) take_next();  // an item with no tile
     }
   };
   int issued = 0;                  // tiles this warp's producer issued (K or V), for the drain of an aborted CTA
