@@ -163,8 +163,7 @@ typedef struct ts_attn_params {
 /*
  * Bytes of device workspace tree_attn_fwd needs for these sizes: 256 bytes
  * for the attention kernel's work-item counter, then the split-prefix
- * partial results, or, with one split per unit, room for up to 128 last-round
- * items cut in halves.  Host-only: launches nothing, safe without a GPU.
+ * partial results.  Host-only: launches nothing, safe without a GPU.
  * Returns 0 for arguments tree_attn_fwd would reject.
  */
 TS_API size_t tree_attn_workspace_size(const ts_attn_params* p);
@@ -196,10 +195,9 @@ TS_API ts_status tree_attn_plan(const ts_attn_params* p, int32_t* chunk_tiles, i
  * workspace: device buffer of at least tree_attn_workspace_size(p) bytes,
  * 256-byte aligned, ZERO-FILLED before its first use: its first 256 bytes
  * hold the counter from which the attention kernel's CTAs (one per SM) take
- * their work items, and with one split per unit its last bytes hold the
- * tickets of the last round's items cut in halves; every call, a timed-out
- * one included, leaves both zero again; the rest is scratch for this call
- * only.  Calls sharing one workspace must be stream-ordered.
+ * their work items, and every call, a timed-out one included, leaves them
+ * zero again; the rest is scratch for this call only.  Calls sharing one
+ * workspace must be stream-ordered.
  * Returns TS_ERR_NULL / TS_ERR_SHAPE / TS_ERR_UNSUPPORTED / TS_ERR_WORKSPACE /
  * TS_ERR_CUDA; a block id outside the pool sets status[b] = TS_ERR_BAD_BLOCK
  * (block 0 is read in its place), a timed-out internal wait sets

@@ -109,15 +109,11 @@ def test_attn_plan_covers_the_prefix_and_sizes_the_workspace(ts, B, N, Hq, Hkv, 
         assert splits == 1
     rows = B * N * Hq
     ws = ts.tree_attn_workspace_size(p)
-    r256 = lambda x: -(-x // 256) * 256
-    # 256 bytes for the persistent kernel's item counter, then the partials;
-    # with one split per unit, room for up to 128 tail items cut in halves
-    # (bf16 rows and lse of both halves, a ticket per softmax warp)
+    # 256 bytes for the persistent kernel's item counter, then the partials
     if splits == 1:
-        items = -(-N * (Hq // Hkv) // 128) * B * Hkv
-        cap = min(items // 2, 128)
-        assert ws == 256 + r256(cap * 2 * 128 * D * 2) + r256(cap * 2 * 128 * 4) + r256(cap * 16)
+        assert ws == 256
     else:
+        r256 = lambda x: -(-x // 256) * 256
         assert ws == 256 + r256(splits * rows * D * 2) + r256(splits * rows * 4)
 
 

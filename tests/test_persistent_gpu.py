@@ -162,90 +162,3 @@ def test_ctas_test_rejects_bad_arguments():
     assert L.tree_attn_fwd_ctas_test(ctypes.byref(p), w, nb, 1, case.B, 0, 2000, None) == -2
     assert L.tree_attn_fwd_ctas_test(ctypes.byref(p), w, nb, 1, 0, -1, 2000, None) == -2
     assert L.tree_attn_fwd_ctas_test(ctypes.byref(p), w, nb, 1, -1, 0, 50, None) == -4
-
-
-# --------------------------------------------------------------------------- tail items
-#
-# With one split per unit, N items on C CTAs leave N mod C for the last round;
-# when that is at most C/2 those items are cut into two halves (the first half
-# of the prefix tiles; the rest and the tree block), and the half that ends
-# second merges the two.  These cases have one split per unit and are run on
-# CTA counts that leave such a last round.
-
-def _tail_case(name, B, N, Hq, Hkv, D, plens, bs=16):
-    g = W.rng(len(name) + 3, name)
-    parent = np.stack([W.tree_random_levels(g, N, 6) for _ in range(B)])
-    return W.build_case(name, 11, parent, plens, Hq=Hq, Hkv=Hkv, D=D, bs=bs, permute=True)
-
-
-def _ticket_bytes_zero(ws):
-    # the counter (first 256 bytes) and the tail tickets (the last region)
-    return ws[:256].cpu().numpy().tobytes() == bytes(256) and not ws[-256:].cpu().numpy().any()
-
-
-TAIL_CASES = [
-    # name, B, N, Hq, Hkv, D, prefix lengths, CTA counts (items n; a tail where n mod C <= C/2)
-    ("tail_d128", 20, 26, 32, 8, 128, [1500 - 37 * i for i in range(20)], [50, 70, 150]),
-    # prefixes of 0-2 tiles: first halves with no tile at all
-    ("tail_short", 40, 20, 16, 4, 128, [(53 * i) % 260 for i in range(40)], [50, 70, 150]),
-    ("tail_d64", 24, 26, 32, 8, 64, [1400 - 41 * i for i in range(24)], [90, 150, 180]),
-]
-
-
-@pytest.mark.parametrize("spec", TAIL_CASES, ids=[c[0] for c in TAIL_CASES])
-def test_tail_items_cut_in_halves(spec):
-    import tree_attention_speculative_gb300 as ts
-    name, B, N, Hq, Hkv, D, plens, ctas_list = spec
-    case = _tail_case(name, B, N, Hq, Hkv, D, plens)
-    step, p, _t = _step(case)
-    plan = ts.tree_attn_plan(p)
-    assert plan["max_splits"] == 1, plan   # one split per unit: the tail rule applies
-    items = -(-N * (Hq // Hkv) // 128) * B * Hkv
-    ws = torch.zeros(ts.tree_attn_workspace_size(p), dtype=torch.uint8, device="cuda")
-    ref, ref_lse = oracle.attention.tree_attention_case(case)
-    tails = 0
-    for ctas in ctas_list:
-        rem = items % ctas
-        tails += 0 < 2 * rem <= ctas
-        for rep in range(2):
-            step.out.zero_()
-            step.lse.zero_()
-            ts.tree_attn_fwd_ctas_test(p, ws, ctas)
-            torch.cuda.synchronize()
-            assert step.status.cpu().tolist() == [0] * case.B
-            _check(step, case, ref, ref_lse, f"{name} on {ctas} CTAs ({items} items), call {rep}")
-            assert _ticket_bytes_zero(ws), "counter or tail tickets not back at zero"
-    assert tails > 0, "no CTA count left a tail to cut"
-
-
-def test_stall_on_tail_halves_keeps_tickets_at_zero():
-    """A stalled sequence whose last-round items are cut in halves: its
-    timeout is reported, every sequence reported fine is right, and the
-    counter and the tail tickets end at zero, so the next ordinary call is
-    right everywhere."""
-    import tree_attention_speculative_gb300 as ts
-    B, N, Hq, Hkv, D = 20, 26, 32, 8, 128
-    case = _tail_case("tail_stall", B, N, Hq, Hkv, D, [1500 - 37 * i for i in range(B)])
-    step, p, _t = _step(case)
-    assert ts.tree_attn_plan(p)["max_splits"] == 1
-    items = -(-N * (Hq // Hkv) // 128) * B * Hkv     # 160, one per (sequence, KV head)
-    ctas = 50                                          # 160 mod 50 = 10: the last 10 items in halves
-    assert 0 < 2 * (items % ctas) <= ctas
-    ws = torch.zeros(ts.tree_attn_workspace_size(p), dtype=torch.uint8, device="cuda")
-    ref, ref_lse = oracle.attention.tree_attention_case(case)
-    for stall_seq in (B - 1, B - 2, 0):   # the last two sequences' items are the tail items
-        step.status.zero_()
-        ts.tree_attn_fwd_ctas_test(p, ws, ctas, stall_seq, 0, 2000)
-        torch.cuda.synchronize()
-        st = step.status.cpu().tolist()
-        assert st[stall_seq] == TS_ERR_TIMEOUT, st
-        assert all(s in (0, TS_ERR_TIMEOUT) for s in st), st
-        assert _ticket_bytes_zero(ws), "counter or tail tickets not back at zero after a timeout"
-        _check(step, case, ref, ref_lse, f"beside stalled sequence {stall_seq}",
-               skip={b for b in range(case.B) if st[b] != 0})
-        step.status.zero_()
-        step.out.zero_()
-        ts.tree_attn_fwd_ctas_test(p, ws, ctas)
-        torch.cuda.synchronize()
-        assert step.status.cpu().tolist() == [0] * case.B
-        _check(step, case, ref, ref_lse, f"call after stalling sequence {stall_seq}")

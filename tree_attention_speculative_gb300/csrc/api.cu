@@ -102,17 +102,8 @@ AttnPlan plan_attn(const ts_attn_params* p) {
   const size_t nrows = (size_t)p->B * p->N * p->Hq;
   pl.part_o_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * p->D * 2) : 0;
   pl.part_lse_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * sizeof(float)) : 0;
-  // with one split per unit, room for the tail items: the last round's items
-  // cut in two halves (at most half the CTAs' worth, see attn_tc.cu)
-  const int n_items = pl.row_tiles * pl.max_splits * p->B * p->Hkv;
-  pl.tail_cap = pl.max_splits == 1 ? (n_items / 2 < ATTN_TAIL_CAP ? n_items / 2 : ATTN_TAIL_CAP) : 0;
-  pl.tail_o_bytes = round256((size_t)pl.tail_cap * 2 * ROW_TILE * p->D * 2);
-  pl.tail_lse_bytes = round256((size_t)pl.tail_cap * 2 * ROW_TILE * sizeof(float));
-  pl.tail_ticket_bytes = round256((size_t)pl.tail_cap * 4 * sizeof(unsigned));
-  // the attention kernel's item counter (256 bytes, zero between calls), the
-  // partials, then the tail halves and their tickets (zero between calls)
-  pl.workspace_bytes = ATTN_SCHED_BYTES + pl.part_o_bytes + pl.part_lse_bytes + pl.tail_o_bytes +
-                       pl.tail_lse_bytes + pl.tail_ticket_bytes;
+  // the attention kernel's item counter (256 bytes, zero between calls), then the partials
+  pl.workspace_bytes = ATTN_SCHED_BYTES + pl.part_o_bytes + pl.part_lse_bytes;
   return pl;
 }
 
@@ -262,17 +253,8 @@ ts_status attn_fwd_impl(const ts_attn_params* p, void* workspace, size_t workspa
   a.status = p->status;
   char* ws = static_cast<char*>(workspace);
   a.sched = reinterpret_cast<unsigned*>(ws);
-  size_t off = ATTN_SCHED_BYTES;
-  a.part_o = reinterpret_cast<__nv_bfloat16*>(ws + off);
-  off += pl.part_o_bytes;
-  a.part_lse = reinterpret_cast<float*>(ws + off);
-  off += pl.part_lse_bytes;
-  a.tail_o = reinterpret_cast<__nv_bfloat16*>(ws + off);
-  off += pl.tail_o_bytes;
-  a.tail_lse = reinterpret_cast<float*>(ws + off);
-  off += pl.tail_lse_bytes;
-  a.tail_ticket = reinterpret_cast<unsigned*>(ws + off);
-  a.tail_cap = pl.tail_cap;
+  a.part_o = reinterpret_cast<__nv_bfloat16*>(ws + ATTN_SCHED_BYTES);
+  a.part_lse = reinterpret_cast<float*>(ws + ATTN_SCHED_BYTES + pl.part_o_bytes);
   a.B = p->B; a.N = p->N; a.Hq = p->Hq; a.Hkv = p->Hkv; a.G = p->Hq / p->Hkv; a.D = p->D;
   a.W = ceil_div(p->N, 64);
   a.bs = p->block_size; a.num_blocks = p->num_blocks; a.max_blocks = p->max_blocks;

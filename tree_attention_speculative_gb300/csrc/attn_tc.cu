@@ -143,16 +143,13 @@ struct __align__(1024) Smem {
   int2 item_q[ITEM_Q];
   int items_pub;
   int items_done;
-  int tail_done[4];  // per softmax warp: the last tail half whose ticket it took (for an aborted CTA)
 };
 
 struct TcArgs {
   AttnArgs a;
   int box_rows;   // rows per paged TMA box: gcd(block_size, 128), so a box never crosses a block
   int direct;     // 1: a single split per unit -> write bf16 out (+ lse) directly
-  int n_items;    // items in the counter's numbering: n_whole whole items, then two halves of each tail item
-  int n_whole;    // items taken whole
-  int n_tail;     // items of the last round cut in two halves (one split per unit, persistent CTAs)
+  int n_items;    // row_tiles * max_splits * B * Hkv work items
   int nodes_per_tile;  // ROW_TILE / G
   int out32;           // the output (or the partials) start on a 32-byte boundary
   // the launch's divisors, for divisions on the device's critical paths
@@ -166,18 +163,10 @@ struct TcArgs {
 // spread over the whole order instead of gathering at its end (numbered
 // split-major, the last splits of the longest prefixes were taken last and
 // ran on alone: 103 against 93 us on 16 paged prefixes of 1-16K tokens).
-//
-// Tail items.  With one split per unit, N items on C persistent CTAs leave the
-// last round N mod C items for C CTAs.  When N mod C <= C/2 those items are
-// each cut into two halves (the first half of the prefix tiles; the rest and
-// the tree block), numbered after the whole items so that they are taken
-// last; the two halves are merged (LSE-weighted, like the split combine) by
-// whichever finishes second.  The last round then takes half as long.
 struct ItemPos {
   int rt, split, b, g;
 };
 __device__ __forceinline__ ItemPos item_pos(int it, const TcArgs& t) {
-  if (it >= t.n_whole) it = t.n_whole + ((it - t.n_whole) >> 1);  // the whole item a half belongs to
   ItemPos p;
   const int rs = t.fd_rt.div(it);
   p.rt = it - rs * t.a.row_tiles;
@@ -195,8 +184,6 @@ struct Item {
   int t_begin;   // first prefix tile of the split
   int n_prefix;  // prefix tiles of this split
   int n_tiles;   // + tree tiles on the sequence's last split
-  int half;      // -1: a whole item; 0 or 1: that half of tail item `tail`
-  int tail;
   bool work;     // false: the split lies past this sequence's prefix
   bool p_ok;     // false: the device prefix length had to be clamped
 };
@@ -213,23 +200,6 @@ __device__ __forceinline__ Item make_item(int it, int p_dev, const TcArgs& t) {
   I.work = I.pos.split < ns;
   I.n_prefix = max(0, min(tiles, I.t_begin + a.chunk_tiles) - I.t_begin);
   I.n_tiles = I.n_prefix + ((I.pos.split == ns - 1) ? ceil_div(a.N, KV_TILE) : 0);
-  I.half = -1;
-  I.tail = 0;
-  if (it >= t.n_whole) {
-    // half 0: the first n_prefix/2 prefix tiles; half 1: the rest and the
-    // tree block (so half 1 is never empty; half 0 is when n_prefix < 2)
-    I.half = (it - t.n_whole) & 1;
-    I.tail = (it - t.n_whole) >> 1;
-    const int h0 = I.n_prefix >> 1;
-    if (I.half == 0) {
-      I.n_prefix = h0;
-      I.n_tiles = h0;
-    } else {
-      I.t_begin += h0;
-      I.n_prefix -= h0;
-      I.n_tiles -= h0;
-    }
-  }
   return I;
 }
 
@@ -352,7 +322,6 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     sm.pv_done = 0;
     sm.items_pub = 0;
     sm.items_done = 0;
-    for (int q = 0; q < 4; ++q) sm.tail_done[q] = -1;
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
     for (int i = 0; i < C::NSTK; ++i) {
@@ -865,10 +834,8 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         break;
       }
       tc_fence_after();
-      // only half 0 of a tail item whose prefix has fewer than 2 tiles is empty
-      const bool empty = I.n_tiles == 0;
-      const float inv = empty ? 0.f : 1.f / l_run;
-      const float lse2 = empty ? NEG_INF : m_run + __log2f(l_run);
+      const float inv = 1.f / l_run;
+      const float lse2 = m_run + __log2f(l_run);
       const size_t orow = ((size_t)b * a.N + node) * a.Hq + h;
       // The CTA's last item goes to the idle K ring (every QK has completed
       // before the last PV could start) as bf16 TMA boxes of 64 columns (one
@@ -876,14 +843,9 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       // chunks (c % 64) / 8 .. +3 of box c / 64, chunk k of row r at
       // k ^ (r % 8) (the 128-byte swizzle, conflict-free for these writes).
       // Any other item writes its rows straight to global memory (the rings
-      // carry the next items' tiles); a tail half writes all 128 rows of its
-      // slot, for the half that finishes second to merge.
-      const bool tail = I.half >= 0;
-      const bool to_stage = e_next.x < 0 && !tail;
-      const int slot_row = (I.tail * 2 + I.half) * ROW_TILE + r;
-      __nv_bfloat16* dst = tail ? a.tail_o + (size_t)slot_row * D
-                                : (args.direct ? a.out + orow * D : a.part_o + ((size_t)split * rows_all + orow) * D);
-      const bool wide = tail || args.out32;  // 32-byte aligned rows
+      // carry the next items' tiles), 16 bytes a store.
+      const bool to_stage = e_next.x < 0;
+      __nv_bfloat16* dst = args.direct ? a.out + orow * D : a.part_o + ((size_t)split * rows_all + orow) * D;
       // The loop is kept rolled: unrolled, it changed how the softmax loop
       // above was compiled, which then ran 10% slower on long prefixes.
 #pragma unroll 1
@@ -894,17 +856,17 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         uint8_t* srow = stage + (c / 64) * (ROW_TILE * 128) + r * 128;
         uint32_t w[16];  // the 32 columns as bf16 pairs
 #pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2)
-          w[e2] = empty ? 0u : pack_bf16x2(__uint_as_float(u[2 * e2]) * inv, __uint_as_float(u[2 * e2 + 1]) * inv);
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
         if (to_stage) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             *reinterpret_cast<uint4*>(srow + ((((c % 64) / 8 + q) ^ (r & 7)) << 4)) =
                 make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        } else if (active || tail) {
-          // a row's 64 bytes here: two 32-byte stores where the rows are
+        } else if (active) {
+          // a row's 64 bytes here: two 32-byte stores where the output is
           // 32-byte aligned (each a whole DRAM sector), else four of 16
-          if (wide) {
+          if (args.out32) {
             st_global_v8(dst + c, w);
             st_global_v8(dst + c + 16, w + 8);
           } else {
@@ -914,60 +876,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
           }
         }
       }
-      if (tail) {
-        a.tail_lse[slot_row] = lse2;
-        // this warp's 32 rows are out: take the warp's ticket of the item
-        __threadfence();
-        __syncwarp();
-        unsigned old = 0;
-        unsigned* ticket = a.tail_ticket + I.tail * 4 + (warp & 3);
-        if (lane == 0) old = atomicAdd(ticket, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (lane == 0) *reinterpret_cast<volatile int*>(&sm.tail_done[warp & 3]) = e.x;
-        if (old == 1) {
-          // the other half has finished too: merge the two, weighted by their
-          // lse (half 1 holds the tree block, so its lse is finite)
-          __threadfence();
-          const int other = (I.tail * 2 + (I.half ^ 1)) * ROW_TILE + r;
-          const float lo = __ldcg(a.tail_lse + other);
-          const float mx = fmaxf(lse2, lo);
-          const float ws = ex2(lse2 - mx), wo = ex2(lo - mx);
-          const float norm = 1.f / (ws + wo);
-          const float fs = ws * norm * inv, fo = wo * norm;
-          const uint4* od = reinterpret_cast<const uint4*>(a.tail_o + (size_t)other * D);
-          __nv_bfloat16* orow_p = a.out + orow * D;
-#pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t u[32];
-            tmem_ld32(tmem + lane_base + TMEM_O + c, u);
-            tmem_ld_wait();
-            uint4 ov[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ov[q] = __ldcg(od + c / 8 + q);
-            const uint32_t* o32 = reinterpret_cast<const uint32_t*>(ov);
-            uint32_t w[16];
-#pragma unroll
-            for (int e2 = 0; e2 < 16; ++e2) {
-              const float s0 = empty ? 0.f : __uint_as_float(u[2 * e2]), s1 = empty ? 0.f : __uint_as_float(u[2 * e2 + 1]);
-              const float o0 = __uint_as_float(o32[e2] << 16), o1 = __uint_as_float(o32[e2] & 0xFFFF0000u);
-              w[e2] = pack_bf16x2(s0 * fs + o0 * fo, s1 * fs + o1 * fo);
-            }
-            if (active) {
-              if (args.out32) {
-                st_global_v8(orow_p + c, w);
-                st_global_v8(orow_p + c + 16, w + 8);
-              } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  reinterpret_cast<uint4*>(orow_p + c)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-              }
-            }
-          }
-          if (active && a.lse) a.lse[orow] = (mx + __log2f(ws + wo)) * 0.69314718055994531f;
-          __syncwarp();
-          if (lane == 0) atomicExch(ticket, 0u);  // back to zero for the next call
-        }
-      } else if (active) {
+      if (active) {
         if (args.direct) {
           if (a.lse) a.lse[orow] = lse2 * 0.69314718055994531f;
         } else {
@@ -1030,20 +939,10 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     // holds, and (so that the counter still ends at zero) every item it
     // takes from now on.
     if (threadIdx.x == 0) {
-      // A tail half also takes, for every softmax warp that had not taken
-      // it yet, that warp's ticket of the item, so that the other half still
-      // finds its count complete and every ticket ends the call at zero.
       auto report = [&](int it) {
-        if (it < 0) return;
+        if (it < 0 || !a.status) return;
         const Item I = make_item(it, a.prefix_len[item_pos(it, args).b], args);
-        if (I.work && a.status) a.status[I.pos.b] = TS_ERR_TIMEOUT;
-        if (I.half >= 0) {
-          for (int q = 0; q < 4; ++q) {
-            if (sm.tail_done[q] == it) continue;
-            unsigned* ticket = a.tail_ticket + I.tail * 4 + q;
-            if (atomicAdd(ticket, 1u) == 1u) atomicExch(ticket, 0u);
-          }
-        }
+        if (I.work) a.status[I.pos.b] = TS_ERR_TIMEOUT;
       };
       const int pub = sm.items_pub, done = sm.items_done;
       for (int k = done; k < pub && k < done + ITEM_Q; ++k) report(sm.item_q[k % ITEM_Q].x);
@@ -1088,10 +987,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   t.box_rows = KV_TILE;  // gcd(block_size, 128): block sizes are multiples of 16
   while (a.bs % t.box_rows != 0) t.box_rows >>= 1;
   t.direct = a.max_splits == 1;
-  const int n_items = a.row_tiles * a.max_splits * a.B * a.Hkv;
-  t.n_items = n_items;
-  t.n_whole = n_items;
-  t.n_tail = 0;
+  t.n_items = a.row_tiles * a.max_splits * a.B * a.Hkv;
   t.nodes_per_tile = ROW_TILE / a.G;
   t.out32 = (reinterpret_cast<uintptr_t>(t.direct ? (const void*)a.out : (const void*)a.part_o) & 31) == 0;
   t.fd_rt = FastDiv::make(a.row_tiles);
@@ -1152,18 +1048,9 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   // layer at 512 rows a unit: 789 against 757 us).
   int ctas = sm_count();
   if (ctas <= 0) return cudaErrorInvalidDevice;
-  if (a.G * a.N < 256) ctas = n_items;
+  if (a.G * a.N < 256) ctas = t.n_items;
   if (a.max_ctas > 0 && a.max_ctas < ctas) ctas = a.max_ctas;
-  if (ctas > n_items) ctas = n_items;
-  // tail items: with one split per unit on persistent CTAs, a last round of
-  // at most half the CTAs is cut into halves (taken last: numbered last)
-  const int rem = n_items % ctas;
-  if (t.direct && ctas < n_items && rem > 0 && 2 * rem <= ctas && rem <= a.tail_cap) {
-    t.n_tail = rem;
-    t.n_whole = n_items - rem;
-    t.n_items = n_items + rem;
-  }
-  dim3 grid(ctas);
+  dim3 grid(t.n_items < ctas ? t.n_items : ctas);
   return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt, m_o,
                     m_po);
 }

@@ -115,12 +115,6 @@ struct AttnArgs {
   unsigned* sched;         // item counter of the persistent attention kernel: zero before and after a call
   __nv_bfloat16* part_o;  // [max_splits, B*N*Hq, D] bf16, normalised partial outputs
   float* part_lse;  // [max_splits, B*N*Hq] fp32, base-2 log-sum-exp of each partial
-  // Tail items (one split per unit, persistent CTAs): at most tail_cap items of
-  // the last round are cut into two halves, merged by the half that ends second.
-  __nv_bfloat16* tail_o;  // [tail_cap, 2, ROW_TILE, D] bf16, each half's normalised rows
-  float* tail_lse;        // [tail_cap, 2, ROW_TILE] base-2 lse of each half's rows
-  unsigned* tail_ticket;  // [tail_cap, 4] halves done, per softmax warp; zero between calls
-  int tail_cap;
   int B, N, Hq, Hkv, G, D, W;
   int bs, num_blocks, max_blocks;
   float scale_log2;  // softmax scale * log2(e)
@@ -144,13 +138,10 @@ struct AttnPlan {
   int max_splits;
   int tree_split;
   int row_tiles;
-  int tail_cap;
   size_t part_o_bytes;
   size_t part_lse_bytes;
-  size_t tail_o_bytes, tail_lse_bytes, tail_ticket_bytes;
   size_t workspace_bytes;
 };
-constexpr int ATTN_TAIL_CAP = 128;  // tail items a workspace has room for (a last round on up to 256 SMs)
 
 cudaError_t launch_ancestry(const int32_t* parent, const int32_t* prefix_len, int B, int N,
                             uint64_t* anc, int32_t* depth, int32_t* pos, int32_t* status,
