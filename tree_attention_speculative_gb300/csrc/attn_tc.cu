@@ -357,13 +357,24 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   // The producers fetch the first item's prefix length and first
   // block-table entries together (volatile loads, issued where written), so
   // the two latencies overlap.
-  const bool grabber = warp == PRODUCER_WARP;
-  const int p_first = grabber ? ld_global_early(a.prefix_len + pos0.b) : 0;
+  //
+  // With one CTA per item (the grid as large as the item count) nothing is
+  // taken from the counter and nothing goes through the queue: every role
+  // reads the prefix length itself and works on item blockIdx.x alone (the
+  // queue's hand-over was measured to add ~1 us to such a CTA's start).
+  const bool single = (int)gridDim.x == n_items;
+  const bool grabber = warp == PRODUCER_WARP && !single;
+  const int p_first = (grabber || single) ? ld_global_early(a.prefix_len + pos0.b) : 0;
   const int blk_first = producer ? ld_global_early(blk_first_addr) : 0;
+  const bool single_work = single && make_item(first, p_first, args).work;
 
-  // Entry k of the item queue (every role but the K producer): false if the
-  // wait gave up.
+  // Entry k of the item queue (every role but the K producer; with one CTA
+  // per item, every role): false if the wait gave up.
   auto queue_entry = [&](int k, int2& e) -> bool {
+    if (single) {
+      e = (k == 0 && single_work) ? make_int2(first, p_first) : make_int2(-1, 0);
+      return true;
+    }
     if (!wait_count(&sm.items_pub, k + 1, ctl)) return false;
     const volatile int* q = reinterpret_cast<volatile int*>(&sm.item_q[k % ITEM_Q]);
     e.x = q[0];
@@ -382,7 +393,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   // but has not published yet (-1: none), and whether the counter said
   // nothing was left.
   int held = -1;
-  bool exhausted = false;
+  bool exhausted = single;  // nothing to take from the counter
 
   // ------------------------------------------------------------ K or V producer
   // One warp streams the K tiles, another the V tiles: a single warp issues a
@@ -411,10 +422,10 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     int jg = 0;               // tiles issued, over every item
     // K producer: the item in hand and its prefix length
     int cand = first, cand_p = p_first;
-    held = first;
+    if (grabber) held = first;
     for (int k = 0;; ++k) {
       int it, p_dev;
-      if (!is_v) {
+      if (grabber) {
         // skip empty splits (a short prefix), taking the next item each time
         for (;;) {
           if (cand < 0 || make_item(cand, cand_p, args).work) break;
@@ -540,8 +551,9 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         ++q_issued;
       };
       // The CTA's first item is `first` unless that split is empty: its Q
-      // tile needs no prefix length, so it is loaded at once.
-      load_q(pos0);
+      // tile needs no prefix length, so it is loaded at once (with one CTA
+      // per item, only if the split has work).
+      if (!single || single_work) load_q(pos0);
       for (int k = 0; ok; ++k) {
         int2 e;
         if (!(ok = queue_entry(k, e))) break;
@@ -604,6 +616,9 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         }
         if (ok) mma_commit(&sm.q_empty);  // Q no longer read once these QKs complete
       }
+      // A Q tile loaded for nothing (the first split was empty and no other
+      // item came) must land before the CTA may exit.
+      if (ok && q_issued > q_landed && wait_bar(&sm.q_full, (q_issued - 1) & 1, ctl)) ++q_landed;
     }
   } else if (warp == PV_WARP) {
     if (lane == 0) {
@@ -944,8 +959,8 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         const Item I = make_item(it, a.prefix_len[item_pos(it, args).b], args);
         if (I.work) a.status[I.pos.b] = TS_ERR_TIMEOUT;
       };
-      const int pub = sm.items_pub, done = sm.items_done;
-      for (int k = done; k < pub && k < done + ITEM_Q; ++k) report(sm.item_q[k % ITEM_Q].x);
+      const int pub = single ? (single_work ? 1 : 0) : sm.items_pub, done = sm.items_done;
+      for (int k = done; k < pub && k < done + ITEM_Q; ++k) report(single ? first : sm.item_q[k % ITEM_Q].x);
       report(held);
       while (!exhausted) {
         const int it = take_item();
