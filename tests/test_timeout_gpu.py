@@ -47,10 +47,13 @@ def test_attention_wait_runs_out_and_reports_timeout(stall_seq, stall_tile):
     step.ancestry(t["parent"], t["prefix_len"])
     p = step._params(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["prefix_len"], t["k_tree"],
                      t["v_tree"])
-    # the sequence's first split holds more than stall_tile tiles, so its CTAs
-    # do reach the withheld tile
+    # the longest split of the sequence holds more than stall_tile tiles (its
+    # ceil(tiles / chunk) splits differ by one tile at most), so its CTAs do
+    # reach the withheld tile
     plan = ts.tree_attn_plan(p)
-    assert min(plan["chunk_tiles"], -(-int(case.prefix_len[stall_seq]) // 128)) > stall_tile, plan
+    tiles = -(-int(case.prefix_len[stall_seq]) // 128)
+    ps = -(-tiles // plan["chunk_tiles"])
+    assert -(-tiles // ps) > stall_tile, plan
     ws = torch.zeros(ts.tree_attn_workspace_size(p), dtype=torch.uint8, device="cuda")
     ts.tree_attn_fwd_stall_test(p, ws, stall_seq, stall_tile, 2000)
     torch.cuda.synchronize()     # the call returns by itself: no hang, no fault

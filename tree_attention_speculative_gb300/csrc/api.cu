@@ -1,4 +1,5 @@
 // C ABI: argument validation, split planning, launches.  See include/treespec.h.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -44,7 +45,8 @@ ts_status check_attn(const ts_attn_params* p) {
 }
 
 // Split plan.  Every (unit, row tile) is one chain of 128-token KV tiles; a
-// split cuts the chain into CTAs of `chunk_tiles` tiles.  The tree block rides
+// sequence's prefix is cut into ceil(tiles / chunk_tiles) splits of near-equal
+// length (at most `chunk_tiles` tiles each).  The tree block rides
 // on the last prefix split of a unit, or (tree_split) on a CTA of its own that
 // runs beside the prefix splits.  The attention kernel holds one CTA per SM,
 // so the time of a plan is about
@@ -98,6 +100,35 @@ AttnPlan plan_attn(const ts_attn_params* p) {
   for (int b = 0; b < p->B; ++b) {
     const int ns = num_splits(p->prefix_len_host[b], pl.chunk_tiles, pl.tree_split);
     pl.max_splits = ns > pl.max_splits ? ns : pl.max_splits;
+  }
+  // The order of the work items: every (sequence, split) pair, longest
+  // first by the host's prefix lengths, so that the short ones (splits of
+  // short prefixes, a tree split) are taken last and fill in beside the
+  // long ones instead of starting after them.  Pairs with no work by the
+  // host's lengths come last (the device's own lengths decide).
+  pl.n_order = 0;
+  if ((long long)p->B * pl.max_splits <= ATTN_ORDER_MAX) {
+    int len[ATTN_ORDER_MAX], idx[ATTN_ORDER_MAX];
+    uint32_t pair[ATTN_ORDER_MAX];
+    int n = 0;
+    for (int b = 0; b < p->B; ++b) {
+      const int tiles = prefix_tiles(p->prefix_len_host[b]);
+      const int ps = ceil_div(tiles, pl.chunk_tiles);
+      const int ns = num_splits(p->prefix_len_host[b], pl.chunk_tiles, pl.tree_split);
+      for (int s = 0; s < pl.max_splits; ++s) {
+        int l = s < ps ? split_start(tiles, ps, s + 1) - split_start(tiles, ps, s) : 0;
+        if (s == ns - 1) l += tree_tiles;
+        const int start = s < ps ? split_start(tiles, ps, s) : 0;
+        pair[n] = ((uint32_t)b << ORDER_B_SHIFT) | ((uint32_t)s << ORDER_SPLIT_SHIFT) |
+                  (uint32_t)(start < ORDER_START_MASK ? start : ORDER_START_MASK);
+        len[n] = l;
+        idx[n] = n;
+        ++n;
+      }
+    }
+    std::stable_sort(idx, idx + n, [&](int x, int y) { return len[x] > len[y]; });
+    for (int e = 0; e < n; ++e) pl.order[e] = pair[idx[e]];
+    pl.n_order = n;
   }
   const size_t nrows = (size_t)p->B * p->N * p->Hq;
   pl.part_o_bytes = pl.max_splits > 1 ? round256((size_t)pl.max_splits * nrows * p->D * 2) : 0;
@@ -268,6 +299,8 @@ ts_status attn_fwd_impl(const ts_attn_params* p, void* workspace, size_t workspa
   a.stall_seq = stall_seq;
   a.stall_tile = stall_tile;
   a.max_ctas = max_ctas;
+  a.n_order = pl.n_order;
+  a.order_host = pl.order;
   cudaStream_t s = (cudaStream_t)stream;
   if (prepare_device() != cudaSuccess) return TS_ERR_CUDA;
   if (launch_attn_tc(a, s) != cudaSuccess) return TS_ERR_CUDA;

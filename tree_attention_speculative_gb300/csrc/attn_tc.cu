@@ -154,26 +154,43 @@ struct TcArgs {
   int out32;           // the output (or the partials) start on a 32-byte boundary
   // the launch's divisors, for divisions on the device's critical paths
   FastDiv fd_rt, fd_ms, fd_hkv, fd_chunk, fd_bs, fd_g;
+  int n_order;  // 0, or B * max_splits entries in order[]
+  uint32_t order[ATTN_ORDER_MAX];  // (sequence, split, first tile), packed as ORDER_* says, in taking order
 };
 
-// A work item: row tile rt of unit (b, g), split `split`.  Items are numbered
-// unit-major, then split, then row tile: CTAs that take items one after the
-// other take the row tiles of a unit side by side (they read the same K/V
-// tiles at about the same time, from L2), and the splits of long prefixes are
-// spread over the whole order instead of gathering at its end (numbered
-// split-major, the last splits of the longest prefixes were taken last and
-// ran on alone: 103 against 93 us on 16 paged prefixes of 1-16K tokens).
+// A work item: row tile rt of unit (b, g), split `split`.  The row tiles of
+// a unit are numbered side by side, so that CTAs taking items one after the
+// other read the same K/V tiles at about the same time (from L2).  With an
+// order table, items go (sequence, split) pair by pair in the table's order
+// (longest first), the KV heads of a pair next to each other; without one,
+// unit-major, then split.  Numbered split-major instead, the last splits of
+// the longest prefixes were taken last and ran on alone (103 against 93 us
+// on 16 paged prefixes of 1-16K tokens).
+// start_hint: the split's first prefix tile by the host's prefix length
+// (the device's may differ; its block-table entries are loaded before the
+// device's is known, and checked against it when used).
 struct ItemPos {
-  int rt, split, b, g;
+  int rt, split, b, g, start_hint;
 };
 __device__ __forceinline__ ItemPos item_pos(int it, const TcArgs& t) {
   ItemPos p;
   const int rs = t.fd_rt.div(it);
   p.rt = it - rs * t.a.row_tiles;
-  const int unit = t.fd_ms.div(rs);
-  p.split = rs - unit * t.a.max_splits;
-  p.b = t.fd_hkv.div(unit);
-  p.g = unit - p.b * t.a.Hkv;
+  if (t.n_order) {
+    const int e = t.fd_hkv.div(rs);
+    p.g = rs - e * t.a.Hkv;
+    const uint32_t v = t.order[e];
+    p.b = (int)(v >> ORDER_B_SHIFT);
+    p.split = (int)((v >> ORDER_SPLIT_SHIFT) & ORDER_SPLIT_MASK);
+    const int h = (int)(v & ORDER_START_MASK);
+    p.start_hint = h == ORDER_START_MASK ? p.split * t.a.chunk_tiles : h;
+  } else {
+    const int unit = t.fd_ms.div(rs);
+    p.split = rs - unit * t.a.max_splits;
+    p.b = t.fd_hkv.div(unit);
+    p.g = unit - p.b * t.a.Hkv;
+    p.start_hint = p.split * t.a.chunk_tiles;
+  }
   return p;
 }
 
@@ -196,10 +213,11 @@ __device__ __forceinline__ Item make_item(int it, int p_dev, const TcArgs& t) {
   // num_splits(I.P, chunk_tiles, tree_split), without its division
   const int ps = t.fd_chunk.div(tiles + a.chunk_tiles - 1);
   const int ns = a.tree_split ? ps + 1 : (ps == 0 ? 1 : ps);
-  I.t_begin = I.pos.split * a.chunk_tiles;
-  I.work = I.pos.split < ns;
-  I.n_prefix = max(0, min(tiles, I.t_begin + a.chunk_tiles) - I.t_begin);
-  I.n_tiles = I.n_prefix + ((I.pos.split == ns - 1) ? ceil_div(a.N, KV_TILE) : 0);
+  const int s = I.pos.split;
+  I.work = s < ns;
+  I.t_begin = s < ps ? split_start(tiles, ps, s) : tiles;
+  I.n_prefix = s < ps ? split_start(tiles, ps, s + 1) - I.t_begin : 0;
+  I.n_tiles = I.n_prefix + ((s == ns - 1) ? ceil_div(a.N, KV_TILE) : 0);
   return I;
 }
 
@@ -300,7 +318,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     for (int hh = 0; hh < C::HALVES; ++hh) tma_prefetch_4d(&tm_q, 64 * hh, pos0.g * a.G, pos0.rt * args.nodes_per_tile, pos0.b);
     if (a.max_blocks > 0) {
       // the 16-byte piece holding the entry, through the bulk-copy unit
-      const int idx = args.fd_bs.div(pos0.split * a.chunk_tiles * KV_TILE);
+      const int idx = args.fd_bs.div(pos0.start_hint * KV_TILE);
       const int* row0 = a.block_table + (size_t)pos0.b * a.max_blocks;
       const uintptr_t e = reinterpret_cast<uintptr_t>(row0 + (idx < a.max_blocks ? idx : a.max_blocks - 1));
       bulk_prefetch_l2(reinterpret_cast<const void*>(e & ~uintptr_t(15)), 16);
@@ -312,7 +330,7 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
   const bool producer = (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) && a.max_blocks > 0;
   const int* blk_first_addr = a.block_table;
   if (producer) {
-    const int t0 = (pos0.split * a.chunk_tiles + lane / g_boxes) * KV_TILE + (lane % g_boxes) * g_box;
+    const int t0 = (pos0.start_hint + lane / g_boxes) * KV_TILE + (lane % g_boxes) * g_box;
     const int idx = args.fd_bs.div(t0);
     blk_first_addr = a.block_table + (size_t)pos0.b * a.max_blocks + (idx < a.max_blocks ? idx : a.max_blocks - 1);
   }
@@ -471,7 +489,9 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       // box (L % boxes) of tile (L / boxes) of a group of 32/boxes tiles; the
       // next group is loaded (one coalesced read) when the current one starts,
       // so the table's load latency hides behind several tiles of TMA issue.
-      const bool use_first = it == first;
+      // (the entries loaded at the start were for the host's prefix length;
+      // if the device's moves the split's start, they are loaded again here)
+      const bool use_first = it == first && t_begin == I.pos.start_hint;
       auto load_group = [&](int grp) -> int {
         const int tile = grp * g_tpg + (lane >> lg_boxes);
         const int t0 = (t_begin + tile) * KV_TILE + koff;
@@ -1011,6 +1031,8 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   t.fd_chunk = FastDiv::make(a.chunk_tiles);
   t.fd_bs = FastDiv::make(a.bs);
   t.fd_g = FastDiv::make(a.G);
+  t.n_order = (a.n_order == a.B * a.max_splits && a.n_order <= ATTN_ORDER_MAX && a.order_host) ? a.n_order : 0;
+  for (int e = 0; e < t.n_order; ++e) t.order[e] = a.order_host[e];
   CUtensorMap m_q, m_kc, m_vc, m_kt, m_vt;
   // q [B, N, Hq, D]: dims (D, Hq, N, B); box (64, G, 128/G, 1) = 128 packed rows
   {

@@ -72,14 +72,24 @@ struct FastDiv {
 };
 
 // Number of prefix tiles of a sequence, and how many splits its prefix is cut
-// into when every split takes `chunk_tiles` tiles.  The tree block rides on
-// the LAST split of a sequence: with tree_split = 0 that is the last prefix
-// split (a sequence with no prefix still has one split for it); with
+// into when no split takes more than `chunk_tiles` tiles.  The tree block
+// rides on the LAST split of a sequence: with tree_split = 0 that is the last
+// prefix split (a sequence with no prefix still has one split for it); with
 // tree_split = 1 it is one more split of its own, with no prefix tiles.
 __host__ __device__ inline int prefix_tiles(int P) { return ceil_div(P, KV_TILE); }
 __host__ __device__ inline int num_splits(int P, int chunk_tiles, int tree_split) {
   const int ps = ceil_div(prefix_tiles(P), chunk_tiles);
   return tree_split ? ps + 1 : (ps == 0 ? 1 : ps);
+}
+// First prefix tile of split s (0 <= s <= ps) when a sequence's `tiles` prefix
+// tiles are cut into ps = ceil(tiles / chunk_tiles) splits of near-equal
+// length (they differ by one tile at most, so none exceeds chunk_tiles).  A
+// fixed chunk would leave the remainder in one short split; equal splits
+// keep the work items of a ragged batch closer in length.  Split s holds
+// tiles [split_start(s), split_start(s + 1)).  tiles <= 2^23 (P <= 2^30) and
+// s <= ps <= 256 (the planner's limit), so the product fits in 32 bits.
+__host__ __device__ inline int split_start(int tiles, int ps, int s) {
+  return ps > 0 ? (int)(((unsigned)tiles * (unsigned)s) / (unsigned)ps) : 0;
 }
 
 // The prefix length a kernel may use for sequence b: the device value, clamped
@@ -129,7 +139,22 @@ struct AttnArgs {
   unsigned long long wait_limit_ns;
   int stall_seq, stall_tile;
   int max_ctas;  // > 0: at most this many CTAs of the persistent kernel (testing); else one per SM
+  // The order of the attention kernel's work items (host array, read when
+  // the launch is made): every (sequence, split) pair once, longest first by
+  // the host's prefix lengths, packed as the ORDER_* constants say.  n_order
+  // = 0: no table (items in unit-major order).
+  int n_order;
+  const uint32_t* order_host;
 };
+// At most this many (sequence, split) pairs are ordered by a table (so b and
+// split each fit in 8 bits); a launch with more keeps the unit-major order.
+// An entry packs b (bits 24-31), split (bits 15-23) and the split's first
+// prefix tile by the host's prefix length (bits 0-14; all ones if larger).
+constexpr int ATTN_ORDER_MAX = 256;
+constexpr int ORDER_B_SHIFT = 24;
+constexpr int ORDER_SPLIT_SHIFT = 15;
+constexpr uint32_t ORDER_SPLIT_MASK = 0x1ffu;
+constexpr int ORDER_START_MASK = 0x7fff;
 constexpr unsigned long long ATTN_WAIT_LIMIT_NS = 200000000ull;  // 200 ms: far above any legitimate wait
 constexpr size_t ATTN_SCHED_BYTES = 256;  // head of the attention workspace: the item counter
 
@@ -141,6 +166,8 @@ struct AttnPlan {
   size_t part_o_bytes;
   size_t part_lse_bytes;
   size_t workspace_bytes;
+  int n_order;  // 0 or B * max_splits (see AttnArgs::order_host)
+  uint32_t order[ATTN_ORDER_MAX];
 };
 
 cudaError_t launch_ancestry(const int32_t* parent, const int32_t* prefix_len, int B, int N,
