@@ -1077,15 +1077,13 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
     if (!encode_bf16_sw128(&m_po, a.part_o, 5, dims, str, box)) return cudaErrorInvalidValue;
   }
   // One CTA per SM (each holds ~225 KB of shared memory), or one per item
-  // when there are fewer.  Below the ridge point (G*N query rows per unit
-  // share each K/V byte, so G*N is the flop-per-byte intensity; the ridge is
-  // ~260 on this GPU) the plan streams HBM, and there one CTA per item, left
-  // to the hardware's own scheduling, was measured faster (16 paged prefixes
-  // of 1-16K tokens, 104 rows a unit: 88.0 against 91.5 us; a 70B-shaped
-  // layer at 512 rows a unit: 789 against 757 us).
+  // when there are fewer.  With the items taken longest first, this also
+  // beat one CTA per item (left to the hardware's own scheduling) on
+  // HBM-bound plans: on 16 paged prefixes of 1-16K tokens, 86.7-87.0
+  // against 89.7 us (a CTA goes on to its next item in ~2.7 us, where a new
+  // CTA took ~7.4 us to its first tile).
   int ctas = sm_count();
   if (ctas <= 0) return cudaErrorInvalidDevice;
-  if (a.G * a.N < 256) ctas = t.n_items;
   if (a.max_ctas > 0 && a.max_ctas < ctas) ctas = a.max_ctas;
   dim3 grid(t.n_items < ctas ? t.n_items : ctas);
   return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt, m_o,
