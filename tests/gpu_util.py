@@ -17,7 +17,7 @@ SMALL = [
     ("w3_192_nodes", 1, 192, 2, 1, 128, [200], 16, "levels"),
     ("w4_256_nodes", 1, 256, 1, 1, 64, [0], 16, "random"),
     ("contiguous_2k", 2, 26, 8, 2, 128, [2048, 2048], 2048, "widths"),
-    ("tree_on_last_split", 5, 130, 8, 8, 128, [3000, 2963, 2926, 2889, 2852], 16, "levels"),
+    ("tree_on_last_split", 5, 130, 8, 8, 128, [6000, 5963, 5926, 5889, 5852], 16, "levels"),
     ("one_split_per_unit", 16, 26, 32, 8, 128, [1500 - 37 * i for i in range(16)], 16, "widths"),
     # block sizes that neither divide a 128-token tile nor are multiples of it
     ("bs48", 2, 37, 8, 2, 128, [300, 1000], 48, "random"),

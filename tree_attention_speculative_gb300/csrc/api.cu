@@ -50,7 +50,8 @@ ts_status check_attn(const ts_attn_params* p) {
 // on the last prefix split of a unit, or (tree_split) on a CTA of its own that
 // runs beside the prefix splits.  The attention kernel holds one CTA per SM,
 // so the time of a plan is about
-//     waves * (chunk + per-CTA overhead) [+ tree tiles] + cost of the partials,
+//     waves * (chunk + per-CTA overhead) [+ tree tiles]
+//       [+ the combine kernel's launch + cost of the partials, when split],
 // in units of one tile's work on one SM (about 0.5 us).  The partials are
 // written and read back once (bf16 O + fp32 lse per split, about 2D + 4 bytes
 // a row) and priced at twice those bytes at the measured HBM rate: at the
@@ -70,6 +71,9 @@ AttnPlan plan_attn(const ts_attn_params* p) {
   const double rows = (double)p->B * p->N * p->Hq;
   const double tile_bytes_equiv = 3.6e6;  // HBM bytes moved in one tile-time
   const double cta_overhead = 1.5;        // prologue + epilogue, in tile-times
+  // A split plan also runs the combine kernel: its launch, its wait for the
+  // attention kernel and its own round trip cost about 2 us whatever its size.
+  const double combine_launch = 4.0;
   double best = 1e300;
   int best_chunk = max_tiles, best_ts = 0;
   for (int ts = 0; ts <= 1; ++ts) {
@@ -85,7 +89,7 @@ AttnPlan plan_attn(const ts_attn_params* p) {
       }
       const double waves = (double)((ctas + PLAN_SMS - 1) / PLAN_SMS);
       double cost = waves * (chunk + cta_overhead) + (ts ? 0 : tree_tiles);
-      if (splits > 1) cost += 2.0 * splits * rows * 2.0 * (p->D * 2.0 + 4.0) / tile_bytes_equiv;
+      if (splits > 1) cost += combine_launch + 2.0 * splits * rows * 2.0 * (p->D * 2.0 + 4.0) / tile_bytes_equiv;
       if (cost < best) {
         best = cost;
         best_chunk = chunk;
