@@ -111,6 +111,23 @@ def test_attention_combine_group_boundaries(plens):
     np.testing.assert_allclose(step.lse.cpu().numpy(), ref_lse, rtol=0, atol=LSE_ATOL)
 
 
+def test_attention_combine_of_few_splits_d64():
+    """Plans of 2..4 splits are merged by the combine's 16-channel form (two
+    16-byte pieces a lane, splits in groups of 4); with D = 64 a row is 4 lanes."""
+    import tree_attention_speculative_gb300 as ts
+    g = W.rng(21, "c16")
+    plens = [3000, 2900, 400, 2000] * 4
+    parent = np.stack([W.tree_random_levels(g, 20, 5) for _ in plens])
+    case = W.build_case("c16", 21, parent, plens, Hq=8, Hkv=8, D=64, bs=16, permute=True)
+    step, t = run_case(case)
+    p = step._params(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["prefix_len"], t["k_tree"], t["v_tree"])
+    assert 2 <= ts.tree_attn_plan(p)["max_splits"] <= 4
+    ref, ref_lse = oracle.attention.tree_attention_case(case)
+    assert step.status.cpu().tolist() == [0] * case.B
+    assert_close_attention(out_f64(step), ref, "few splits, D = 64")
+    np.testing.assert_allclose(step.lse.cpu().numpy(), ref_lse, rtol=0, atol=LSE_ATOL)
+
+
 def test_attention_hot_keys_softmax_range():
     case = W.build_case("hot", 3, W.tree_random_levels(W.rng(1, "h"), 48, 6), [700, 1500], Hq=8, Hkv=2,
                         D=128, bs=64, permute=True, hot_key_frac=0.05, hot_key_scale=8.0)
