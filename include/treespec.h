@@ -18,7 +18,7 @@
  *                           the same for several roots per sequence
  *   tree_verify_stochastic  temperature verification by rejection sampling
  *   tree_commit_accepted    append the accepted path to the paged cache
- *   tree_attn_workspace_size, tree_attn_plan, tree_verify_workspace_size
+ *   tree_attn_workspace_size, tree_attn_plan, tree_attn_plan_order, tree_verify_workspace_size
  *                           host-only queries: workspace bytes, split plan
  *
  * Sources (web pages on the method):
@@ -171,7 +171,8 @@ TS_API size_t tree_attn_workspace_size(const ts_attn_params* p);
 /*
  * tree_attn_plan — how tree_attn_fwd will cut the work for these arguments
  * (host only, launches nothing).  The prefix of every (sequence, KV head,
- * 128-row tile) is cut into splits of *chunk_tiles 128-token tiles;
+ * 128-row tile) of T 128-token tiles is cut into ceil(T / *chunk_tiles)
+ * splits of near-equal length (split s starts at tile floor(T s / splits));
  * *max_splits is the split count of the longest sequence (the grid's split
  * extent), and *tree_split is 1 when the tree block runs as a split of its
  * own rather than on the last prefix split.  With *max_splits == 1 the
@@ -181,6 +182,22 @@ TS_API size_t tree_attn_workspace_size(const ts_attn_params* p);
  */
 TS_API ts_status tree_attn_plan(const ts_attn_params* p, int32_t* chunk_tiles, int32_t* max_splits,
                                 int32_t* tree_split);
+
+/*
+ * tree_attn_plan_order — the order in which the attention kernel takes its
+ * work items for these arguments (host only, launches nothing): every
+ * (sequence, split) pair once, longest first by prefix_len_host (ties in
+ * sequence, then split order).  Entry e of `order` is
+ * (b << 24) | (split << 15) | first_tile, first_tile being the split's first
+ * prefix tile by prefix_len_host (0x7fff when larger; 0 for a split with no
+ * prefix tiles).  *count receives the number of pairs, B * max_splits, or 0
+ * when there are more than 256 (the kernel then takes the items sequence by
+ * sequence, split by split); at most `cap` entries are written.  `order` may
+ * be NULL when cap is 0.
+ * Returns TS_ERR_NULL / TS_ERR_SHAPE / TS_ERR_UNSUPPORTED like tree_attn_fwd,
+ * and TS_ERR_SHAPE when cap is negative or smaller than *count.
+ */
+TS_API ts_status tree_attn_plan_order(const ts_attn_params* p, uint32_t* order, int32_t cap, int32_t* count);
 
 /*
  * tree_attn_fwd — the attention layer of the batched verification pass

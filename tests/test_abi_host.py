@@ -248,3 +248,67 @@ def test_forest_calls_reject_before_launch(ts):
     assert L.tree_verify_greedy_forest(*bad) == -1
     bad = list(args); bad[13] = need - 1
     assert L.tree_verify_greedy_forest(*bad) == -8
+
+
+def _expected_pairs(P, chunk, splits, tsplit, tree_tiles):
+    """(length in tiles, first prefix tile) of every (sequence, split) pair when
+    each prefix of T tiles is cut into ceil(T / chunk) splits of near-equal
+    length, split s starting at floor(T s / splits), and the tree block rides on
+    the sequence's last split (or a split of its own)."""
+    out = {}
+    for b, p in enumerate(P):
+        tiles = -(-p // 128)
+        ps = -(-tiles // chunk)
+        ns = ps + 1 if tsplit else max(ps, 1)
+        for s in range(splits):
+            start = tiles * s // ps if s < ps else 0
+            n = (tiles * (s + 1) // ps - start) if s < ps else 0
+            if s == ns - 1:
+                n += tree_tiles
+            out[(b, s)] = (n, start)
+    return out
+
+
+@pytest.mark.parametrize("B,N,Hq,Hkv,P", [
+    (16, 26, 32, 8, (1207, 1427, 1497, 1964, 2939, 4413, 5913, 6798, 7843, 7953, 8097, 8622, 10608, 11850, 13284,
+                     15195)),
+    (8, 33, 8, 2, (0, 17, 1000, 4096, 130, 2500, 3999, 1)),
+    (1, 64, 32, 8, (4096,)),
+    (4, 192, 32, 8, (131072,) * 4),
+    (6, 30, 8, 2, (700, 3000, 130, 1900, 0, 2500)),
+    (256, 3, 2, 1, tuple(16 * (i % 7) for i in range(256))),
+])
+def test_attn_plan_order_is_every_pair_longest_first(ts, B, N, Hq, Hkv, P):
+    p = _params(ts, B=B, N=N, Hq=Hq, Hkv=Hkv, D=128 if N > 3 else 64, bs=16, P=P)
+    plan = ts.tree_attn_plan(p)
+    order = ts.tree_attn_plan_order(p)
+    pairs = B * plan["max_splits"]
+    assert len(order) == (pairs if pairs <= 256 else 0)
+    exp = _expected_pairs(P, plan["chunk_tiles"], plan["max_splits"], plan["tree_split"], -(-N // 128))
+    got = [(e >> 24, (e >> 15) & 0x1FF, e & 0x7FFF) for e in order]
+    assert sorted((b, s) for b, s, _ in got) == sorted(exp)          # every pair exactly once
+    lens = [exp[(b, s)][0] for b, s, _ in got]
+    assert lens == sorted(lens, reverse=True)                        # longest first
+    for i in range(1, len(got)):                                     # ties keep sequence, then split order
+        if lens[i] == lens[i - 1]:
+            assert got[i][:2] > got[i - 1][:2]
+    for b, s, start in got:                                          # the first tile of each split
+        assert start == min(exp[(b, s)][1], 0x7FFF)
+    for b in range(B):                                               # splits cover the prefix, none over the chunk
+        tiles = -(-P[b] // 128)
+        ps = -(-tiles // plan["chunk_tiles"])
+        sizes = [tiles * (s + 1) // ps - tiles * s // ps for s in range(ps)]
+        assert sum(sizes) == tiles and all(0 < x <= plan["chunk_tiles"] for x in sizes)
+
+
+def test_attn_plan_order_counts_without_a_table_past_256_pairs(ts):
+    P = tuple(16 * (i % 5) + 2000 * (i == 7) for i in range(300))
+    p = _params(ts, B=300, N=3, Hq=2, Hkv=1, D=64, bs=16, P=P)
+    assert ts.tree_attn_plan(p)["max_splits"] >= 2
+    assert ts.tree_attn_plan_order(p) == []
+    n = ctypes.c_int32(-1)
+    assert ts.lib().tree_attn_plan_order(ctypes.byref(p), None, 0, ctypes.byref(n)) == 0 and n.value == 0
+    small = _params(ts, B=2, N=26, Hq=32, Hkv=8, D=128, bs=16, P=(1000, 3000))
+    assert ts.lib().tree_attn_plan_order(ctypes.byref(small), None, 0, ctypes.byref(n)) == -2   # cap 0 < count
+    assert ts.lib().tree_attn_plan_order(ctypes.byref(small), None, -1, ctypes.byref(n)) == -2
+    assert ts.lib().tree_attn_plan_order(ctypes.byref(small), None, 0, None) == -1

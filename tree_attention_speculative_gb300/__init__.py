@@ -20,7 +20,8 @@ from ._build import LIB as LIB_PATH
 
 __all__ = [
     "TreeSpecError", "lib", "ts_status_str", "tree_build_ancestry", "AttnParams", "attn_params",
-    "tree_attn_workspace_size", "tree_attn_plan", "tree_attn_fwd", "tree_verify_workspace_size", "tree_verify_greedy",
+    "tree_attn_workspace_size", "tree_attn_plan", "tree_attn_plan_order", "tree_attn_fwd",
+    "tree_verify_workspace_size", "tree_verify_greedy",
     "tree_verify_greedy_noalloc", "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic",
     "tree_build_ancestry_forest", "tree_verify_greedy_forest", "NOALLOC_SCRATCH_BYTES",
     "STATUS",
@@ -54,7 +55,8 @@ class AttnParams(ctypes.Structure):
 _LIB: Optional[ctypes.CDLL] = None
 
 # every symbol include/treespec.h declares
-EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_plan", "tree_attn_fwd",
+EXPORTS = ("ts_status_str", "tree_build_ancestry", "tree_attn_workspace_size", "tree_attn_plan", "tree_attn_plan_order",
+           "tree_attn_fwd",
            "tree_verify_workspace_size", "tree_verify_greedy", "tree_verify_greedy_noalloc",
            "tree_commit_accepted", "tree_verify_stochastic", "tree_build_dynamic", "tree_build_ancestry_forest",
            "tree_verify_greedy_forest", "tree_attn_fwd_stall_test", "tree_attn_fwd_ctas_test")
@@ -79,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.tree_attn_workspace_size.restype = sz
         L.tree_attn_plan.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp]
         L.tree_attn_plan.restype = i32
+        L.tree_attn_plan_order.argtypes = [ctypes.POINTER(AttnParams), vp, i32, vp]
+        L.tree_attn_plan_order.restype = i32
         L.tree_attn_fwd.argtypes = [ctypes.POINTER(AttnParams), vp, sz, vp]
         L.tree_attn_fwd.restype = i32
         L.tree_attn_fwd_stall_test.argtypes = [ctypes.POINTER(AttnParams), vp, sz, i32, i32, ctypes.c_uint32, vp]
@@ -175,6 +179,15 @@ def tree_attn_plan(params: AttnParams) -> dict:
     _check(lib().tree_attn_plan(ctypes.byref(params), ctypes.byref(c), ctypes.byref(s), ctypes.byref(t)),
            "tree_attn_plan")
     return {"chunk_tiles": c.value, "max_splits": s.value, "tree_split": t.value}
+
+
+def tree_attn_plan_order(params: AttnParams) -> list:
+    """The packed (sequence, split, first tile) entries in the order the
+    attention kernel takes its items (host only); [] when it orders none."""
+    n = ctypes.c_int32()
+    buf = (ctypes.c_uint32 * 256)()  # the most pairs the kernel orders
+    _check(lib().tree_attn_plan_order(ctypes.byref(params), buf, 256, ctypes.byref(n)), "tree_attn_plan_order")
+    return [int(buf[i]) for i in range(n.value)]
 
 
 def tree_attn_fwd(params: AttnParams, workspace: torch.Tensor, stream=None) -> None:

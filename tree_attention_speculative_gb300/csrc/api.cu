@@ -263,6 +263,18 @@ ts_status tree_attn_plan(const ts_attn_params* p, int32_t* chunk_tiles, int32_t*
   return TS_OK;
 }
 
+ts_status tree_attn_plan_order(const ts_attn_params* p, uint32_t* order, int32_t cap, int32_t* count) {
+  const ts_status st = check_attn(p);
+  if (st != TS_OK) return st;
+  if (!count || (cap > 0 && !order)) return TS_ERR_NULL;
+  if (cap < 0) return TS_ERR_SHAPE;
+  const AttnPlan pl = plan_attn(p);
+  *count = pl.n_order;
+  if (cap < pl.n_order) return TS_ERR_SHAPE;
+  for (int e = 0; e < pl.n_order; ++e) order[e] = pl.order[e];
+  return TS_OK;
+}
+
 }  // extern "C"
 
 namespace ts {
