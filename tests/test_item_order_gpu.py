@@ -12,7 +12,7 @@ oracle where host and device disagree, and where no order table is used:
   loaded again), and sequences have more or fewer splits than the table
   expects (splits the table ranks last, as empty, have work);
 - a batch with more (sequence, split) pairs than one table holds: items go
-  in unit-major order.
+  in unit-major order; and one with exactly as many as it holds.
 """
 import numpy as np
 import pytest
@@ -49,7 +49,7 @@ def _run(case, host_len, ctas=None):
         ts.tree_attn_fwd_ctas_test(p, ws, ctas)
     torch.cuda.synchronize()
     assert ws[:256].cpu().numpy().tobytes() == bytes(256), "item counter not back at zero"
-    return step, ts.tree_attn_plan(p)
+    return step, dict(ts.tree_attn_plan(p), pairs=len(ts.tree_attn_plan_order(p)))
 
 
 def _check(step, case, what):
@@ -81,5 +81,17 @@ def test_more_pairs_than_one_table_holds():
     parent = np.stack([W.tree_random_levels(g, 3, 2) for _ in plens])
     case = W.build_case("pairs", 12, parent, plens, Hq=2, Hkv=1, D=64, bs=16, permute=True)
     step, plan = _run(case, plens)
-    assert case.B * plan["max_splits"] > 256, plan
+    assert case.B * plan["max_splits"] > 256 and plan["pairs"] == 0, plan
     _check(step, case, "unit-major order")
+
+
+def test_exactly_one_full_table_of_pairs():
+    """256 (sequence, split) pairs, the most one order table holds: sequence
+    255 is the largest the entries' 8-bit field carries."""
+    g = W.rng(14, "t256")
+    plens = [int(x) for x in g.integers(0, 250, 256)]
+    parent = np.stack([W.tree_random_levels(g, 3, 2) for _ in plens])
+    case = W.build_case("t256", 14, parent, plens, Hq=2, Hkv=1, D=64, bs=16, permute=True)
+    step, plan = _run(case, plens)
+    assert plan["pairs"] == 256 and case.B * plan["max_splits"] == 256, plan
+    _check(step, case, "a full order table")
