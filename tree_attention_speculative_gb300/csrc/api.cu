@@ -56,8 +56,9 @@ ts_status check_attn(const ts_attn_params* p) {
 // written and read back once (bf16 O + fp32 lse per split, about 2D + 4 bytes
 // a row) and priced at twice those bytes at the measured HBM rate: at the
 // plain price the planner picked 7 splits for the batched-serving workload
-// (16 sequences, paged prefixes of 1-16K), which ran 5% slower than 4.  The plan with the smallest estimate wins; ties keep the
-// tree on the last prefix split.
+// (16 sequences, paged prefixes of 1-16K), which ran 5% slower than 4.  The
+// plan with the smallest estimate wins; ties keep the tree on the last prefix
+// split.
 AttnPlan plan_attn(const ts_attn_params* p) {
   AttnPlan pl{};
   const int G = p->Hq / p->Hkv;
