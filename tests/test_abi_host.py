@@ -124,6 +124,14 @@ def test_attn_plan_gives_the_tree_its_own_split_on_one_wave(ts):
     assert plan["max_splits"] == 1 and plan["tree_split"] == 0
 
 
+def test_attn_plan_keeps_one_split_when_a_combine_would_cost_more(ts):
+    """A split plan pays the combine kernel's launch whatever its size: the
+    5-node demo tree on a 16-token prefix runs as one split with the tree
+    block on it (a split of its own would save one tile and add a kernel)."""
+    plan = ts.tree_attn_plan(_params(ts, B=1, N=5, Hq=2, Hkv=2, D=64, bs=16, P=(16,)))
+    assert plan == {"chunk_tiles": 1, "max_splits": 1, "tree_split": 0}
+
+
 def _plan_of(ts, name, B, N, Hq, Hkv, D, plens, bs, tree):
     return ts.tree_attn_plan(_params(ts, B=B, N=N, Hq=Hq, Hkv=Hkv, D=D, bs=bs, P=tuple(plens)))
 
