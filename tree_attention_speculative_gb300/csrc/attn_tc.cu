@@ -43,8 +43,11 @@
 //              masks, tracks the running max/sum, writes P (bf16) back over S,
 //              rescales O when the max moves by more than 2^20 (exact: the final
 //              normalisation uses the same running max).  At the end of an
-//              item each thread normalises its row of O to bf16 and stores it
-//              (32-byte stores): the output itself, or this split's partial.
+//              item each thread normalises its row of O to bf16 and stores it:
+//              the output itself, or this split's partial.  After the CTA's
+//              last item the K ring is idle, so the rows go there instead, in
+//              the 128-byte-swizzled layout of a TMA box, and one thread
+//              stores the boxes.
 //   With QK and PV on two issuers the next tile's QK^T and this tile's PV
 //   run while the softmax works.  Each control warp shares its sub-partition
 //   with a softmax warp, and the scheduler keeps issuing from a ready compute
@@ -282,7 +285,8 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tm_q,
           const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
-          const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
+          const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
+          const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_po) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -681,6 +685,11 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
     const size_t rows_all = (size_t)a.B * a.N * a.Hq;
     int jg = 0;  // tiles, over every item
     bool ok = true;
+    // the CTA's last item ends in the idle K ring, stored by TMA boxes after
+    // the loop (every softmax thread reaches that barrier, whatever happens)
+    bool staged = false;
+    ItemPos last_pos{0, 0, 0, 0};
+    uint8_t* stage = &sm.k[0][0];
     int2 e;
     ok = queue_entry(0, e);
     for (int k = 0; ok && e.x >= 0; ++k) {
@@ -863,10 +872,14 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
       const float inv = 1.f / l_run;
       const float lse2 = m_run + __log2f(l_run);
       const size_t orow = ((size_t)b * a.N + node) * a.Hq + h;
-      // Each thread writes its row straight to global memory.  (Staging the
-      // CTA's last item in the idle K ring and storing it with TMA boxes was
-      // measured slower: the CTA then waited for the bulk store to read its
-      // source before it could exit.)
+      // The CTA's last item goes to the idle K ring (every QK has completed
+      // before the last PV could start) as bf16 TMA boxes of 64 columns (one
+      // per D half), each 128 rows of 128 bytes: columns c .. c+31 are
+      // chunks (c % 64) / 8 .. +3 of box c / 64, chunk k of row r at
+      // k ^ (r % 8) (the 128-byte swizzle, conflict-free for these writes).
+      // Any other item writes its rows straight to global memory (the rings
+      // carry the next items' tiles), 16 bytes a store.
+      const bool to_stage = e_next.x < 0;
       __nv_bfloat16* dst = args.direct ? a.out + orow * D : a.part_o + ((size_t)split * rows_all + orow) * D;
       // The loop is kept rolled: unrolled, it changed how the softmax loop
       // above was compiled, which then ran 10% slower on long prefixes.
@@ -875,11 +888,17 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
         uint32_t u[32];
         tmem_ld32(tmem + lane_base + TMEM_O + c, u);
         tmem_ld_wait();
+        uint8_t* srow = stage + (c / 64) * (ROW_TILE * 128) + r * 128;
         uint32_t w[16];  // the 32 columns as bf16 pairs
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           w[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
-        if (active) {
+        if (to_stage) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(srow + ((((c % 64) / 8 + q) ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        } else if (active) {
           // a row's 64 bytes here: two 32-byte stores where the output is
           // 32-byte aligned (each a whole DRAM sector), else four of 16
           if (args.out32) {
@@ -899,12 +918,34 @@ k_attn_tc(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorM
           a.part_lse[(size_t)split * rows_all + orow] = lse2;
         }
       }
-      // O has been read: the next item's first PV may overwrite it (it
-      // waits for that item's first P, which follows in program order)
-      tc_fence_before();
-      __syncwarp();
-      if (r == 0) asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.items_done)), "r"(k + 1) : "memory");
+      if (to_stage) {
+        fence_proxy_async();
+        staged = true;
+        last_pos = I.pos;
+      } else {
+        // O has been read: the next item's first PV may overwrite it (it
+        // waits for that item's first P, which follows in program order)
+        tc_fence_before();
+        __syncwarp();
+        if (r == 0) asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.items_done)), "r"(k + 1) : "memory");
+      }
       e = e_next;
+    }
+    // every softmax thread reaches this barrier, whatever happened above
+    const bool all_staged = named_barrier_and(1, SOFTMAX_THREADS, staged);
+    if (all_staged && r == 0) {
+      // rows of nodes >= N fall outside the tensor and are not written
+      const int node0 = last_pos.rt * args.nodes_per_tile;
+      for (int hh = 0; hh < C::HALVES; ++hh) {
+        if (args.direct)
+          tma_store_4d(&tm_o, stage + hh * (ROW_TILE * 128), 64 * hh, last_pos.g * a.G, node0, last_pos.b);
+        else
+          tma_store_5d(&tm_po, stage + hh * (ROW_TILE * 128), 64 * hh, last_pos.g * a.G, node0, last_pos.b,
+                       last_pos.split);
+      }
+      bulk_commit_group();
+      bulk_wait_read_all();
+      asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.items_done)), "r"(0x7fffffff) : "memory");
     }
   }
 
@@ -1018,6 +1059,23 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
     if (!encode_bf16_sw128(&m_kt, a.k_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
     if (!encode_bf16_sw128(&m_vt, a.v_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
+  // output boxes of 64 columns: bf16 out [B, N, Hq, D] like q (direct), or the
+  // bf16 partial of each split [max_splits, B, N, Hq, D]
+  CUtensorMap m_o, m_po;
+  std::memset(&m_o, 0, sizeof(m_o));
+  std::memset(&m_po, 0, sizeof(m_po));
+  if (t.direct) {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.N, (uint64_t)a.B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)a.Hq * D * 2, (uint64_t)a.N * a.Hq * D * 2};
+    const uint32_t box[4] = {64, (uint32_t)a.G, (uint32_t)(ROW_TILE / a.G), 1};
+    if (!encode_bf16_sw128(&m_o, a.out, 4, dims, str, box)) return cudaErrorInvalidValue;
+  } else {
+    const uint64_t dims[5] = {(uint64_t)D, (uint64_t)a.Hq, (uint64_t)a.N, (uint64_t)a.B, (uint64_t)a.max_splits};
+    const uint64_t str[4] = {(uint64_t)D * 2, (uint64_t)a.Hq * D * 2, (uint64_t)a.N * a.Hq * D * 2,
+                             (uint64_t)a.B * a.N * a.Hq * D * 2};
+    const uint32_t box[5] = {64, (uint32_t)a.G, (uint32_t)(ROW_TILE / a.G), 1, 1};
+    if (!encode_bf16_sw128(&m_po, a.part_o, 5, dims, str, box)) return cudaErrorInvalidValue;
+  }
   // One CTA per SM (each holds ~225 KB of shared memory), or one per item
   // when there are fewer.  With the items taken longest first, this also
   // beat one CTA per item (left to the hardware's own scheduling) on
@@ -1028,7 +1086,8 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   if (ctas <= 0) return cudaErrorInvalidDevice;
   if (a.max_ctas > 0 && a.max_ctas < ctas) ctas = a.max_ctas;
   dim3 grid(t.n_items < ctas ? t.n_items : ctas);
-  return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt);
+  return launch_pdl(k_attn_tc<D>, grid, dim3(NUM_THREADS), smem_bytes<D>(), s, t, m_q, m_kc, m_vc, m_kt, m_vt, m_o,
+                    m_po);
 }
 
 }  // namespace
